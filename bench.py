@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark: attention calls/s of the write-time FP8 ring cache at 757 queries
+over a 5,788-slot ring (48 heads x 128), and ms per 240-call chunk, on GB300.
+
+One step = one four-frame chunk of the production model shape: for each of the
+4 denoising passes and 60 layers, write the chunk's 757 new tokens into the
+layer's ring (RoPE + per-head E4M3 quantisation) and run the attention call of
+the 757 queries over all 5,788 slots; then one position reset (delta rotation of
+every stored key in all 60 layers) that moves the window back by one chunk, so
+positions stay in [0, 5788).  That is every step of the path once per step.
+The rings (4.3 GB) and the 240 distinct (K, V, Q) inputs of a chunk (6.7 GB)
+are far larger than L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own session on its own GPU (the
+method is batch-1 per session; replicas, weak scaling) and rank 0 prints the
+aggregate.  --impl reference times the fp64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L, H, D, C, N_NEW, PREFILL, PASSES = 60, 48, 128, 5788, 757, 5031, 4
+CALLS_PER_CHUNK = L * PASSES
+METRIC = "attention calls/s at 757q×5788-slot FP8 ring cache; ms per 240-call chunk"
+ATTN_FLOP = 4.0 * N_NEW * C * D * H                      # 107.68 GFLOP per call (algorithmic)
+WRITE_BYTES = N_NEW * H * D * (2 + 2) + N_NEW * H * D * 2  # bf16 K,V read + E4M3 K,V codes written
+ROTATE_BYTES = 2.0 * L * H * C * D                        # K codes read + written, all layers
+READTIME_EXTRA_BYTES = C * H * D * (2 + 2) + C * H * D * 2  # bf16 store read + FP8 ring written
+
+# dram bytes per launch measured by ncu (profiles/), valid only for the kernel
+# source they were taken on
+TRAFFIC = {
+    "attention": {"bytes": None, "src_sha256": None},
+}
+
+
+def src_sha(name: str) -> str:
+    path = os.path.join(ROOT, "fp8_ring_kv_cache_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return json.load(open(path)), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+    import synth_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    seed = 21 + 1000 * rank
+    cache = rc.RingKVCache(L, H, D, C, max_write=C)
+    mult = si.outlier_mask(H, D, seed)
+    # the 240 distinct inputs of a chunk, resident in HBM before timing
+    K = torch.empty(PASSES, L, N_NEW, H, D, dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    Q = torch.empty_like(K)
+    for pas in range(PASSES):
+        for layer in range(L):
+            k, v, q = si.chunk_tensors(seed, 0, pas, layer, dev, mult=mult)
+            K[pas, layer], V[pas, layer], Q[pas, layer] = k, v, q
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    kp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, 7), dev, mult)
+    vp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, 8), dev, mult)
+    for layer in range(L):
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+    chunk_pos = np.arange(PREFILL, PREFILL + N_NEW)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def chunk(rec=None):
+        for pas in range(PASSES):
+            for layer in range(L):
+                if rec is not None:
+                    i = rec["i"]
+                    rec["w"][i][0].record(stream)
+                cache.write(layer, K[pas, layer], V[pas, layer], chunk_pos)
+                if rec is not None:
+                    rec["w"][i][1].record(stream)
+                    rec["a"][i][0].record(stream)
+                cache.attend(layer, Q[pas, layer], out)
+                if rec is not None:
+                    rec["a"][i][1].record(stream)
+                    rec["i"] = i + 1
+
+    def step(rec=None):
+        chunk(rec)
+        if rec is not None:
+            j = rec["j"]
+            rec["r"][j][0].record(stream)
+        cache.delta_rotate(-N_NEW)          # the window restarts: oldest stored position -> 0
+        if rec is not None:
+            rec["r"][j][1].record(stream)
+            rec["j"] = j + 1
+
+    for _ in range(args.warmup):
+        step()
+    cache.sync()
+
+    # ---- timed region: K steps, per-kernel events on the launching stream
+    nw = args.steps * CALLS_PER_CHUNK
+    rec = {"w": [(ev(), ev()) for _ in range(nw)], "a": [(ev(), ev()) for _ in range(nw)],
+           "r": [(ev(), ev()) for _ in range(args.steps)], "i": 0, "j": 0}
+    launches0 = cache.launch_count
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(rec)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    cache.sync()
+    launches = cache.launch_count - launches0
+    elapsed_ms = t0.elapsed_time(t1)
+    w_times = [a.elapsed_time(b) * 1e3 for a, b in rec["w"]]
+    a_times = [a.elapsed_time(b) * 1e3 for a, b in rec["a"]]
+    r_times = [a.elapsed_time(b) * 1e3 for a, b in rec["r"]]
+
+    # ---- chunk without a reset (ms per 240-call chunk), same inputs
+    torch.cuda.synchronize()
+    c0, c1 = ev(), ev()
+    c0.record(stream)
+    for _ in range(args.steps):
+        chunk()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chunk_ms = c0.elapsed_time(c1) / args.steps
+    cache.sync()
+    del cache
+
+    # ---- read-time ablation: same chunk, whole-cache RoPE + quantisation per call
+    ab = run_ablation(args, dev, K, V, Q, mult, seed, kp, vp)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(args, dev, K, V, Q, mult, kp, vp)
+
+    # ---- max over ranks
+    if world > 1:
+        t = torch.tensor([elapsed_ms, e2e["elapsed_ms"]], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = e2e["elapsed_ms"]
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]           # fp8 dense = 2x bf16 dense (nominal ratio)
+    hbm = peaks["hbm_gbs"]
+    ms_step = elapsed_ms / args.steps
+    value = world * CALLS_PER_CHUNK * args.steps / (elapsed_ms / 1e3)
+    att_us = statistics.mean(a_times)
+    achieved_tflops = ATTN_FLOP / (att_us * 1e-6) / 1e12
+    w_us = statistics.mean(w_times)
+    r_us = statistics.mean(r_times)
+    tr = TRAFFIC["attention"]
+    traffic = tr["bytes"] if tr["bytes"] is not None and tr["src_sha256"] == src_sha("rc_attention.cu") else None
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "calls/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {
+            "workload": "chunk of 240 calls: 4 passes x 60 layers x (write 757 new tokens + attention of "
+                        "757 queries over 5,788 FP8 slots), 48 heads x 128, then one 60-layer delta rotation",
+            "layers": L, "heads": H, "head_dim": D, "slots": C, "new_tokens": N_NEW, "prefill": PREFILL,
+            "calls_per_step": CALLS_PER_CHUNK, "outliers": "1% of (head, channel) pairs x20 on K and V",
+            "l2": "no flush: 4.3 GB of rings and 6.7 GB of chunk inputs per step exceed the 129 MB L2",
+            "parallelism": f"replicas x{world} (one session per GPU)",
+        },
+        "ms_per_chunk": round(chunk_ms, 4),
+        "roofline": {
+            "bound": "tensor", "kernel": "attention (rc_attend)",
+            "achieved": round(achieved_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved_tflops / fp8_peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal ratio 2)",
+            "per_launch_us": round(att_us, 3), "flop_per_launch": ATTN_FLOP,
+        },
+        "kernels": {
+            "write": {"us": round(w_us, 3), "bytes": WRITE_BYTES,
+                      "gbs": round(WRITE_BYTES / (w_us * 1e-6) / 1e9, 1),
+                      "frac_hbm": round(WRITE_BYTES / (w_us * 1e-6) / 1e9 / hbm, 4),
+                      "note": "event span includes the per-write host launch gap"},
+            "delta_rotate": {"us": round(r_us, 3), "bytes": ROTATE_BYTES,
+                             "gbs": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9, 1),
+                             "frac_hbm": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9 / hbm, 4)},
+            "attention": {"us": round(att_us, 3), "tflops": round(achieved_tflops, 1),
+                          "frac_fp8": round(achieved_tflops / fp8_peak, 4)},
+            "readtime_ablation": ab,
+            "hbm_peak_gbs": hbm, "peak_source": peak_src,
+        },
+        "e2e": {"value": round(world * CALLS_PER_CHUNK * args.steps / (e2e_ms / 1e3), 2), "unit": "calls/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_ms / args.steps, 3)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(calls=args.cpu_calls)
+    return res
+
+
+def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+
+    cache = rc.RingKVCache(L, H, D, C, max_write=C, readtime_ablation=True)
+    for layer in range(L):
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    pos = np.arange(PREFILL, PREFILL + N_NEW)
+    stream = torch.cuda.current_stream()
+
+    def chunk(readtime: bool):
+        for pas in range(PASSES):
+            for layer in range(L):
+                cache.write(layer, K[pas, layer], V[pas, layer], pos)
+                if readtime:
+                    cache.attend_readtime(layer, Q[pas, layer], out)
+                else:
+                    cache.attend(layer, Q[pas, layer], out)
+
+    res = {}
+    for mode in (False, True):
+        chunk(mode)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(max(1, args.steps // 2)):
+            chunk(mode)
+        b.record(stream)
+        torch.cuda.synchronize()
+        res["readtime" if mode else "writetime"] = a.elapsed_time(b) / max(1, args.steps // 2)
+    cache.sync()
+    del cache
+    extra_ms = res["readtime"] - res["writetime"]
+    return {"ms_per_chunk_readtime": round(res["readtime"], 3),
+            "ms_per_chunk_writetime_same_store": round(res["writetime"], 3),
+            "saved_ms_per_chunk": round(extra_ms, 3),
+            "extra_us_per_call": round(extra_ms * 1e3 / CALLS_PER_CHUNK, 3),
+            "extra_bytes_per_call": READTIME_EXTRA_BYTES}
+
+
+def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
+    """The same chunk through the public API with pinned host inputs: every call
+    copies its K, V, Q host->device and its output device->host, inside the
+    timed region, on a copy stream overlapped with the compute stream."""
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+
+    cache = rc.RingKVCache(L, H, D, C, max_write=C)
+    for layer in range(L):
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+    nbuf = 8
+    hk = [K[0, i].cpu().pin_memory() for i in range(nbuf)]
+    hv = [V[0, i].cpu().pin_memory() for i in range(nbuf)]
+    hq = [Q[0, i].cpu().pin_memory() for i in range(nbuf)]
+    hout = [torch.empty(N_NEW, H, D, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dk = [torch.empty_like(K[0, 0]) for _ in range(2)]
+    dv = [torch.empty_like(K[0, 0]) for _ in range(2)]
+    dq = [torch.empty_like(K[0, 0]) for _ in range(2)]
+    dout = [torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    pos = np.arange(PREFILL, PREFILL + N_NEW)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    for e in consumed + drained:
+        e.record(comp)
+
+    def chunk():
+        i = 0
+        for pas in range(PASSES):
+            for layer in range(L):
+                b = i & 1
+                with torch.cuda.stream(copy):
+                    copy.wait_event(consumed[b])
+                    dk[b].copy_(hk[i % nbuf], non_blocking=True)
+                    dv[b].copy_(hv[i % nbuf], non_blocking=True)
+                    dq[b].copy_(hq[i % nbuf], non_blocking=True)
+                    in_ready[b].record(copy)
+                comp.wait_event(in_ready[b])
+                comp.wait_event(drained[b])
+                cache.write(layer, dk[b], dv[b], pos)
+                cache.attend(layer, dq[b], dout[b])
+                consumed[b].record(comp)
+                out_ready[b].record(comp)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(out_ready[b])
+                    hout[b].copy_(dout[b], non_blocking=True)
+                    drained[b].record(copy)
+                i += 1
+
+    for _ in range(args.warmup):
+        chunk()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        chunk()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3
+    cache.sync()
+    del cache
+    per_call_in = 3 * N_NEW * H * D * 2
+    per_call_out = N_NEW * H * D * 4
+    return {"elapsed_ms": ms, "h2d": CALLS_PER_CHUNK * per_call_in, "d2h": CALLS_PER_CHUNK * per_call_out}
+
+
+# ---------------------------------------------------------------- the oracle
+
+def cpu_calls(calls: int, seed: int = 11) -> tuple[float, int, str]:
+    """Time the fp64 oracle on full production calls (prefill untimed; each call =
+    write 757 + attention of 757 queries over 5,788 slots, all 48 heads)."""
+    import numpy as np
+
+    import oracle
+    import synth_inputs as si
+
+    oracle.build()
+    t = si.production_tensors(seed, "cpu")
+    oc = oracle.OracleCache(1, H, D, C)
+    oc.write(0, t["k_prefill"], t["v_prefill"], np.arange(0, PREFILL))
+    times = []
+    for i in range(calls):
+        t0 = time.perf_counter()
+        oc.write(0, t["k_new"], t["v_new"], np.arange(PREFILL, C))
+        oc.attend(0, t["q"])
+        times.append(time.perf_counter() - t0)
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    sample = (f"{calls} full production calls (write 757 tokens + attention 757 x 5,788, 48 heads x 128) "
+              "after an untimed 5,031-token prefill")
+    return statistics.mean(times), cores, sample
+
+
+def cpu_baseline(calls: int) -> dict:
+    t, cores, sample = cpu_calls(calls)
+    return {"value": round(1.0 / t, 5), "unit": "calls/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "s_per_call": round(t, 3)}
+
+
+def run_reference(args, rank: int, world: int) -> dict | None:
+    if rank != 0:
+        return None
+    steps, warmup = args.steps, args.warmup
+    t_w, cores, sample = cpu_calls(max(1, warmup))
+    t, cores, sample = cpu_calls(steps)
+    value = 1.0 / t
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 5), "unit": "calls/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(t * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "one production call per step: write 757 new tokens + attention of 757 queries "
+                               "over 5,788 slots, 48 heads x 128 (the fp64 oracle on the host cores)",
+                   "heads": H, "head_dim": D, "slots": C, "new_tokens": N_NEW, "prefill": PREFILL},
+        "cpu_baseline": {"value": round(value, 5), "unit": "calls/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-calls", type=int, default=3, help="oracle calls timed for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        res = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""ctypes binding of librc.so (include/rc.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls.  Tensors are
+passed as their device addresses; positions are passed as a host int64 array.
+There is no fallback: if librc.so is missing, importing raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librc.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "rc.h")
+
+RC_OK = 0
+RC_ERR_ARG = -1
+RC_ERR_STATE = -2
+RC_ERR_CUDA = -3
+RC_ERR_OOM = -4
+RC_ERR_TIMEOUT = -5
+RC_ERR_UNSUPPORTED = -6
+RC_F_READTIME_ABLATION = 1
+EMPTY = np.iinfo(np.int64).min
+
+
+class RcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {rc_status_string(status)} ({status})")
+
+
+class rc_config(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("slots", ctypes.c_int), ("max_write", ctypes.c_int), ("rope_base", ctypes.c_double),
+                ("flags", ctypes.c_uint)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run fp8_ring_kv_cache_gb300.build.build() (nvcc, sm_103a) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    sig = {
+        "rc_cache_create": ([ctypes.POINTER(rc_config), I, ctypes.POINTER(P)], I),
+        "rc_cache_write": ([P, I, P, P, P, I, P], I),
+        "rc_cache_delta_rotate": ([P, I64, P], I),
+        "rc_attend": ([P, I, P, P, I, P], I),
+        "rc_attend_readtime": ([P, I, P, P, I, P], I),
+        "rc_cache_destroy": ([P], None),
+        "rc_status_string": ([I], ctypes.c_char_p),
+        "rc_cache_sync": ([P], I),
+        "rc_cache_export": ([P, I, P, P, P, P, P, P], I),
+        "rc_cache_export_readtime": ([P, P, P, P, P], I),
+        "rc_cache_occupancy": ([P, I], I),
+        "rc_cache_delta_total": ([P], I64),
+        "rc_cache_launch_count": ([P], I64),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/rc.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rc_\w+)\s*\(", text)))
+
+
+def _check(st: int, what: str) -> None:
+    if st != RC_OK:
+        raise RcError(st, what)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t, dtype, shape, what: str) -> ctypes.c_void_p:
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def rc_status_string(status: int) -> str:
+    return lib.rc_status_string(int(status)).decode()
+
+
+def rc_cache_create(layers: int, heads: int, head_dim: int, slots: int, max_write: int | None = None,
+                    rope_base: float = 10000.0, flags: int = 0, device: int = 0) -> ctypes.c_void_p:
+    cfg = rc_config(layers, heads, head_dim, slots, slots if max_write is None else max_write, rope_base, flags)
+    h = ctypes.c_void_p()
+    _check(lib.rc_cache_create(ctypes.byref(cfg), int(device), ctypes.byref(h)), "rc_cache_create")
+    return h
+
+
+def rc_cache_destroy(h) -> None:
+    lib.rc_cache_destroy(h)
+
+
+def rc_cache_write(h, layer: int, K, V, positions, heads: int, head_dim: int, stream=None) -> None:
+    import torch
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    n = int(pos.shape[0])
+    shape = (n, heads, head_dim)
+    kp = _dev_ptr(K, torch.bfloat16, shape, "K")
+    vp = _dev_ptr(V, torch.bfloat16, shape, "V")
+    _check(lib.rc_cache_write(h, int(layer), kp, vp, pos.ctypes.data_as(ctypes.c_void_p), n, _stream_ptr(stream)),
+           "rc_cache_write")
+
+
+def rc_cache_delta_rotate(h, delta: int, stream=None) -> None:
+    _check(lib.rc_cache_delta_rotate(h, int(delta), _stream_ptr(stream)), "rc_cache_delta_rotate")
+
+
+def rc_attend(h, layer: int, Q, out, heads: int, head_dim: int, stream=None) -> None:
+    import torch
+    n = int(Q.shape[0])
+    qp = _dev_ptr(Q, torch.bfloat16, (n, heads, head_dim), "Q")
+    op = _dev_ptr(out, torch.float32, (n, heads, head_dim), "out")
+    _check(lib.rc_attend(h, int(layer), qp, op, n, _stream_ptr(stream)), "rc_attend")
+
+
+def rc_attend_readtime(h, layer: int, Q, out, heads: int, head_dim: int, stream=None) -> None:
+    import torch
+    n = int(Q.shape[0])
+    qp = _dev_ptr(Q, torch.bfloat16, (n, heads, head_dim), "Q")
+    op = _dev_ptr(out, torch.float32, (n, heads, head_dim), "out")
+    _check(lib.rc_attend_readtime(h, int(layer), qp, op, n, _stream_ptr(stream)), "rc_attend_readtime")
+
+
+def rc_cache_sync(h) -> None:
+    _check(lib.rc_cache_sync(h), "rc_cache_sync")
+
+
+def _np_ptr(a: np.ndarray) -> ctypes.c_void_p:
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def rc_cache_export(h, layer: int, heads: int, head_dim: int, slots: int) -> dict:
+    st = dict(kcodes=np.zeros((heads, slots, head_dim), np.uint8), kscale=np.zeros((heads, slots), np.float32),
+              vcodes=np.zeros((heads, slots, head_dim), np.uint8), vscale=np.zeros((heads, slots), np.float32),
+              pos=np.zeros(slots, np.int64), gid=np.zeros(slots, np.int64))
+    _check(lib.rc_cache_export(h, int(layer), *[_np_ptr(st[k]) for k in
+                                                ("kcodes", "kscale", "vcodes", "vscale", "pos", "gid")]),
+           "rc_cache_export")
+    return st
+
+
+def rc_cache_export_readtime(h, heads: int, head_dim: int, slots: int) -> dict:
+    st = dict(kcodes=np.zeros((heads, slots, head_dim), np.uint8), kscale=np.zeros((heads, slots), np.float32),
+              vcodes=np.zeros((heads, slots, head_dim), np.uint8), vscale=np.zeros((heads, slots), np.float32))
+    _check(lib.rc_cache_export_readtime(h, *[_np_ptr(st[k]) for k in ("kcodes", "kscale", "vcodes", "vscale")]),
+           "rc_cache_export_readtime")
+    return st
+
+
+def rc_cache_occupancy(h, layer: int) -> int:
+    v = lib.rc_cache_occupancy(h, int(layer))
+    if v < 0:
+        raise RcError(v, "rc_cache_occupancy")
+    return v
+
+
+def rc_cache_delta_total(h) -> int:
+    return int(lib.rc_cache_delta_total(h))
+
+
+def rc_cache_launch_count(h) -> int:
+    return int(lib.rc_cache_launch_count(h))
+
+
+class RingKVCache:
+    """Owns one rc_cache handle; methods forward to the C entry points."""
+
+    def __init__(self, layers: int, heads: int, head_dim: int, slots: int, max_write: int | None = None,
+                 rope_base: float = 10000.0, readtime_ablation: bool = False, device: int = 0):
+        self.layers, self.heads, self.head_dim, self.slots = layers, heads, head_dim, slots
+        self.max_write = slots if max_write is None else max_write
+        flags = RC_F_READTIME_ABLATION if readtime_ablation else 0
+        self.handle = rc_cache_create(layers, heads, head_dim, slots, self.max_write, rope_base, flags, device)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            rc_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    def write(self, layer, K, V, positions, stream=None):
+        rc_cache_write(self.handle, layer, K, V, positions, self.heads, self.head_dim, stream)
+
+    def delta_rotate(self, delta, stream=None):
+        rc_cache_delta_rotate(self.handle, delta, stream)
+
+    def attend(self, layer, Q, out, stream=None):
+        rc_attend(self.handle, layer, Q, out, self.heads, self.head_dim, stream)
+
+    def attend_readtime(self, layer, Q, out, stream=None):
+        rc_attend_readtime(self.handle, layer, Q, out, self.heads, self.head_dim, stream)
+
+    def sync(self):
+        rc_cache_sync(self.handle)
+
+    def export(self, layer):
+        return rc_cache_export(self.handle, layer, self.heads, self.head_dim, self.slots)
+
+    def export_readtime(self):
+        return rc_cache_export_readtime(self.handle, self.heads, self.head_dim, self.slots)
+
+    def occupancy(self, layer):
+        return rc_cache_occupancy(self.handle, layer)
+
+    @property
+    def delta_total(self):
+        return rc_cache_delta_total(self.handle)
+
+    @property
+    def launch_count(self):
+        return rc_cache_launch_count(self.handle)

@@ -1,0 +1,599 @@
+// rc_host.cu -- the C ABI (include/rc.h): handle, ring-slot allocator and index
+// math, write-group bookkeeping, RoPE table pool, argument checks, launches,
+// and the canonical export used by the tests.
+//
+// Ring index math (paperdot abstract: "a ring cache"; cpdf.ai "Como rodar 57B
+// em tempo real com batch size 1": the window advances without copies): token
+// at position p lives in slot floormod(p - delta_total, C).  A delta rotation
+// adds delta to every stored position and to delta_total, so no token moves.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "rc.h"
+#include "rc_internal.h"
+#include "rc_layout.h"
+
+using namespace rc;
+
+namespace {
+
+constexpr int kPoolEntries = 4;
+constexpr int64_t kEmpty = INT64_MIN;
+
+struct RopeEntry {
+    bool valid = false;
+    bool arith = false;
+    int64_t p0 = 0;
+    int n = 0;
+    std::vector<int64_t> pos;  // the positions (kept for non-arithmetic keys)
+    uint64_t stamp = 0;
+    float2* d_table = nullptr;  // [max_write][D/2]
+    int64_t* d_pos = nullptr;   // [max_write]
+    int64_t* h_pos = nullptr;   // pinned staging [max_write]
+    cudaEvent_t copied = nullptr;
+    bool copy_pending = false;
+};
+
+}  // namespace
+
+struct rc_cache {
+    rc_config cfg{};
+    int device = 0;
+    int L = 0, H = 0, D = 0, C = 0, T = 0, Cpad = 0, max_write = 0;
+    bool ablation = false;
+    // device memory
+    uint8_t* d_kc = nullptr;
+    uint8_t* d_vt = nullptr;
+    float* d_sk = nullptr;
+    float* d_sv = nullptr;
+    int32_t* d_grp = nullptr;
+    double* d_theta = nullptr;
+    int* d_status = nullptr;
+    __nv_bfloat16* d_kraw = nullptr;
+    __nv_bfloat16* d_vraw = nullptr;
+    float2* d_slot_rope = nullptr;
+    uint8_t* d_rt_kc = nullptr;
+    uint8_t* d_rt_vt = nullptr;
+    float* d_rt_sk = nullptr;
+    float* d_rt_sv = nullptr;
+    RopeEntry pool[kPoolEntries];
+    uint64_t clock = 0;
+    // host mirrors of the ring tables
+    std::vector<int64_t> pos, gid;        // [L][C]
+    std::vector<int32_t> grp;             // [L][C] compact group index, -1 empty
+    std::vector<int> occupancy;           // [L]
+    std::vector<std::vector<int32_t>> refcnt, freelist;  // per layer
+    std::vector<std::vector<int64_t>> last_pos;          // per layer
+    std::vector<int> last_n, last_entry;
+    std::vector<uint32_t> slot_mark;
+    uint32_t mark = 0;
+    std::vector<double> theta;
+    int64_t delta_total = 0, next_gid = 0, launches = 0;
+    cudaStream_t last_stream = nullptr;
+};
+
+namespace {
+
+size_t ring_bytes(const rc_cache* h) {
+    return static_cast<size_t>(h->L) * h->H * h->T * kTileSlots * h->D;
+}
+size_t scale_count(const rc_cache* h) { return static_cast<size_t>(h->L) * h->H * h->Cpad; }
+
+int64_t floormod(int64_t a, int64_t m) {
+    int64_t r = a % m;
+    return r < 0 ? r + m : r;
+}
+
+void free_all(rc_cache* h) {
+    if (!h) return;
+    cudaSetDevice(h->device);
+    cudaFree(h->d_kc);
+    cudaFree(h->d_vt);
+    cudaFree(h->d_sk);
+    cudaFree(h->d_sv);
+    cudaFree(h->d_grp);
+    cudaFree(h->d_theta);
+    cudaFree(h->d_status);
+    cudaFree(h->d_kraw);
+    cudaFree(h->d_vraw);
+    cudaFree(h->d_slot_rope);
+    cudaFree(h->d_rt_kc);
+    cudaFree(h->d_rt_vt);
+    cudaFree(h->d_rt_sk);
+    cudaFree(h->d_rt_sv);
+    for (auto& e : h->pool) {
+        cudaFree(e.d_table);
+        cudaFree(e.d_pos);
+        if (e.h_pos) cudaFreeHost(e.h_pos);
+        if (e.copied) cudaEventDestroy(e.copied);
+    }
+    delete h;
+}
+
+bool is_arith(const int64_t* p, int n) {
+    for (int t = 1; t < n; ++t)
+        if (p[t] != p[0] + t) return false;
+    return true;
+}
+
+// Find or build the RoPE table entry for positions p[0..n).
+int rope_entry(rc_cache* h, const int64_t* p, int n, cudaStream_t s, int* err) {
+    const bool arith = is_arith(p, n);
+    for (int e = 0; e < kPoolEntries; ++e) {
+        RopeEntry& r = h->pool[e];
+        if (!r.valid || r.n != n || r.arith != arith || r.p0 != p[0]) continue;
+        if (!arith && std::memcmp(r.pos.data(), p, sizeof(int64_t) * n) != 0) continue;
+        r.stamp = ++h->clock;
+        return e;
+    }
+    int victim = 0;
+    for (int e = 1; e < kPoolEntries; ++e)
+        if (!h->pool[e].valid || (h->pool[victim].valid && h->pool[e].stamp < h->pool[victim].stamp)) victim = e;
+    if (!h->pool[victim].valid) {
+        for (int e = 0; e < kPoolEntries; ++e)
+            if (!h->pool[e].valid) {
+                victim = e;
+                break;
+            }
+    }
+    RopeEntry& r = h->pool[victim];
+    r.valid = false;
+    RopeTableParams tp{};
+    tp.table = r.d_table;
+    tp.theta = h->d_theta;
+    tp.n = n;
+    tp.half = h->D / 2;
+    if (arith) {
+        tp.pos = nullptr;
+        tp.p0 = p[0];
+        r.pos.clear();
+    } else {
+        if (r.copy_pending) {
+            if (cudaEventSynchronize(r.copied) != cudaSuccess) {
+                *err = RC_ERR_CUDA;
+                return -1;
+            }
+            r.copy_pending = false;
+        }
+        std::memcpy(r.h_pos, p, sizeof(int64_t) * n);
+        if (cudaMemcpyAsync(r.d_pos, r.h_pos, sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaEventRecord(r.copied, s) != cudaSuccess) {
+            *err = RC_ERR_CUDA;
+            return -1;
+        }
+        r.copy_pending = true;
+        r.pos.assign(p, p + n);
+        tp.pos = r.d_pos;
+        tp.p0 = 0;
+    }
+    if (launch_rope_table(tp, s) != cudaSuccess) {
+        *err = RC_ERR_CUDA;
+        return -1;
+    }
+    h->launches += 1;
+    r.valid = true;
+    r.arith = arith;
+    r.p0 = p[0];
+    r.n = n;
+    r.stamp = ++h->clock;
+    return victim;
+}
+
+template <typename T>
+int dmalloc(T** p, size_t count) {
+    if (count == 0) count = 1;
+    return cudaMalloc(reinterpret_cast<void**>(p), sizeof(T) * count) == cudaSuccess ? RC_OK : RC_ERR_OOM;
+}
+
+int check_sticky() {
+    cudaError_t e = cudaPeekAtLastError();
+    return e == cudaSuccess ? RC_OK : RC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rc_status_string(int status) {
+    switch (status) {
+        case RC_OK: return "ok";
+        case RC_ERR_ARG: return "invalid argument";
+        case RC_ERR_STATE: return "call not valid in the cache's current state";
+        case RC_ERR_CUDA: return "CUDA error";
+        case RC_ERR_OOM: return "out of device memory";
+        case RC_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case RC_ERR_UNSUPPORTED: return "unsupported shape or device";
+        default: return "unknown status";
+    }
+}
+
+int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
+    if (!out) return RC_ERR_ARG;
+    *out = nullptr;
+    if (!cfg) return RC_ERR_ARG;
+    if (cfg->layers < 1 || cfg->heads < 1 || cfg->slots < 1 || cfg->max_write < 1 || cfg->max_write > cfg->slots ||
+        !(cfg->rope_base > 1.0))
+        return RC_ERR_ARG;
+    if (cfg->head_dim != 64 && cfg->head_dim != 128) return RC_ERR_UNSUPPORTED;
+    if (cfg->slots > 32768 || cfg->heads > 65535 || cfg->layers > 65535) return RC_ERR_UNSUPPORTED;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return RC_ERR_ARG;
+    cudaDeviceProp prop{};
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return RC_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return RC_ERR_UNSUPPORTED;
+    if (cudaSetDevice(device) != cudaSuccess) return RC_ERR_CUDA;
+
+    rc_cache* h = new (std::nothrow) rc_cache();
+    if (!h) return RC_ERR_OOM;
+    h->cfg = *cfg;
+    h->device = device;
+    h->L = cfg->layers;
+    h->H = cfg->heads;
+    h->D = cfg->head_dim;
+    h->C = cfg->slots;
+    h->T = tiles_of(cfg->slots);
+    h->Cpad = h->T * kTileSlots;
+    h->max_write = cfg->max_write;
+    h->ablation = (cfg->flags & RC_F_READTIME_ABLATION) != 0;
+
+    int st = RC_OK;
+    const size_t rb = ring_bytes(h), sc = scale_count(h);
+    st |= dmalloc(&h->d_kc, rb);
+    st |= dmalloc(&h->d_vt, rb);
+    st |= dmalloc(&h->d_sk, sc);
+    st |= dmalloc(&h->d_sv, sc);
+    st |= dmalloc(&h->d_grp, static_cast<size_t>(h->L) * h->Cpad);
+    st |= dmalloc(&h->d_theta, static_cast<size_t>(h->D / 2));
+    st |= dmalloc(&h->d_status, 1);
+    for (auto& e : h->pool) {
+        st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
+        st |= dmalloc(&e.d_pos, static_cast<size_t>(h->max_write));
+        if (cudaMallocHost(reinterpret_cast<void**>(&e.h_pos), sizeof(int64_t) * h->max_write) != cudaSuccess)
+            st |= RC_ERR_OOM;
+        if (cudaEventCreateWithFlags(&e.copied, cudaEventDisableTiming) != cudaSuccess) st |= RC_ERR_OOM;
+    }
+    if (h->ablation) {
+        const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
+        st |= dmalloc(&h->d_kraw, raw);
+        st |= dmalloc(&h->d_vraw, raw);
+        st |= dmalloc(&h->d_slot_rope, static_cast<size_t>(h->L) * h->Cpad * (h->D / 2));
+        const size_t one = static_cast<size_t>(h->H) * h->T * kTileSlots * h->D;
+        st |= dmalloc(&h->d_rt_kc, one);
+        st |= dmalloc(&h->d_rt_vt, one);
+        st |= dmalloc(&h->d_rt_sk, static_cast<size_t>(h->H) * h->Cpad);
+        st |= dmalloc(&h->d_rt_sv, static_cast<size_t>(h->H) * h->Cpad);
+    }
+    if (st != RC_OK) {
+        free_all(h);
+        cudaGetLastError();  // clear the allocation error
+        return RC_ERR_OOM;
+    }
+    bool ok = cudaMemset(h->d_kc, 0, rb) == cudaSuccess && cudaMemset(h->d_vt, 0, rb) == cudaSuccess &&
+              cudaMemset(h->d_sk, 0, sizeof(float) * sc) == cudaSuccess &&
+              cudaMemset(h->d_sv, 0, sizeof(float) * sc) == cudaSuccess &&
+              cudaMemset(h->d_grp, 0xFF, sizeof(int32_t) * h->L * h->Cpad) == cudaSuccess &&
+              cudaMemset(h->d_status, 0, sizeof(int)) == cudaSuccess;
+    if (ok && h->ablation) {
+        const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
+        ok = cudaMemset(h->d_kraw, 0, raw * 2) == cudaSuccess && cudaMemset(h->d_vraw, 0, raw * 2) == cudaSuccess &&
+             cudaMemset(h->d_slot_rope, 0, sizeof(float2) * h->L * h->Cpad * (h->D / 2)) == cudaSuccess;
+    }
+    h->theta.resize(h->D / 2);
+    for (int i = 0; i < h->D / 2; ++i) h->theta[i] = std::pow(cfg->rope_base, -2.0 * i / h->D);
+    ok = ok && cudaMemcpy(h->d_theta, h->theta.data(), sizeof(double) * (h->D / 2), cudaMemcpyHostToDevice) ==
+                   cudaSuccess;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        free_all(h);
+        return RC_ERR_CUDA;
+    }
+    const size_t lc = static_cast<size_t>(h->L) * h->C;
+    h->pos.assign(lc, kEmpty);
+    h->gid.assign(lc, kEmpty);
+    h->grp.assign(lc, -1);
+    h->occupancy.assign(h->L, 0);
+    h->refcnt.assign(h->L, std::vector<int32_t>(h->C, 0));
+    h->freelist.assign(h->L, std::vector<int32_t>());
+    for (int l = 0; l < h->L; ++l) {
+        h->freelist[l].reserve(h->C);
+        for (int g = h->C - 1; g >= 0; --g) h->freelist[l].push_back(g);
+    }
+    h->last_pos.assign(h->L, std::vector<int64_t>());
+    for (auto& v : h->last_pos) v.reserve(h->max_write);
+    h->last_n.assign(h->L, 0);
+    h->last_entry.assign(h->L, -1);
+    h->slot_mark.assign(h->C, 0);
+    *out = h;
+    return RC_OK;
+}
+
+void rc_cache_destroy(rc_cache* h) {
+    if (!h) return;
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    free_all(h);
+}
+
+int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf16, const int64_t* positions, int n,
+                   void* stream) {
+    if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
+    if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // distinct slots
+    if (++h->mark == 0) {
+        std::fill(h->slot_mark.begin(), h->slot_mark.end(), 0u);
+        h->mark = 1;
+    }
+    for (int t = 0; t < n; ++t) {
+        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        if (h->slot_mark[slot] == h->mark) return RC_ERR_ARG;
+        h->slot_mark[slot] = h->mark;
+    }
+    if (check_sticky() != RC_OK) return RC_ERR_CUDA;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    int err = RC_OK;
+    const int entry = rope_entry(h, positions, n, s, &err);
+    if (entry < 0) return err;
+    const RopeEntry& re = h->pool[entry];
+
+    // write-group bookkeeping: release the groups whose last slot is overwritten
+    const size_t lb = static_cast<size_t>(layer) * h->C;
+    auto& rc = h->refcnt[layer];
+    auto& fl = h->freelist[layer];
+    for (int t = 0; t < n; ++t) {
+        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        const int32_t old = h->grp[lb + slot];
+        if (old >= 0) {
+            if (--rc[old] == 0) fl.push_back(old);
+        } else {
+            h->occupancy[layer] += 1;
+        }
+    }
+    const int32_t g = fl.back();
+    fl.pop_back();
+    rc[g] = n;
+    for (int t = 0; t < n; ++t) {
+        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        h->pos[lb + slot] = positions[t];
+        h->gid[lb + slot] = h->next_gid;
+        h->grp[lb + slot] = g;
+    }
+
+    WriteParams wp{};
+    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D;
+    const size_t lsc = static_cast<size_t>(layer) * h->H * h->Cpad;
+    wp.kc = h->d_kc + lring;
+    wp.vt = h->d_vt + lring;
+    wp.sk = h->d_sk + lsc;
+    wp.sv = h->d_sv + lsc;
+    wp.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
+    wp.K = static_cast<const __nv_bfloat16*>(K_bf16);
+    wp.V = static_cast<const __nv_bfloat16*>(V_bf16);
+    wp.rope = re.d_table;
+    wp.pos = re.arith ? nullptr : re.d_pos;
+    wp.p0 = positions[0];
+    wp.delta_total = h->delta_total;
+    wp.n = n;
+    wp.H = h->H;
+    wp.C = h->C;
+    wp.T = h->T;
+    wp.Cpad = h->Cpad;
+    wp.group = g;
+    if (h->ablation) {
+        const size_t raw = static_cast<size_t>(layer) * h->H * h->Cpad * h->D;
+        wp.kraw = h->d_kraw + raw;
+        wp.vraw = h->d_vraw + raw;
+        wp.slot_rope = h->d_slot_rope + static_cast<size_t>(layer) * h->Cpad * (h->D / 2);
+    }
+    if (launch_write(wp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    h->last_pos[layer].assign(positions, positions + n);
+    h->last_n[layer] = n;
+    h->last_entry[layer] = entry;
+    h->next_gid += 1;
+    h->last_stream = s;
+    return RC_OK;
+}
+
+int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
+    if (!h) return RC_ERR_ARG;
+    if (delta == 0) return RC_OK;
+    if (check_sticky() != RC_OK) return RC_ERR_CUDA;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RotateParams rp{};
+    rp.kc = h->d_kc;
+    rp.sk = h->d_sk;
+    rp.grp = h->d_grp;
+    rp.H = h->H;
+    rp.C = h->C;
+    rp.T = h->T;
+    rp.Cpad = h->Cpad;
+    for (int i = 0; i < h->D / 2; ++i) {
+        const double ang = static_cast<double>(delta) * h->theta[i];
+        rp.cs[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+    }
+    if (launch_rotate(rp, h->D, h->L, s, h->d_status) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    for (size_t i = 0; i < h->pos.size(); ++i)
+        if (h->pos[i] != kEmpty) h->pos[i] += delta;
+    for (int l = 0; l < h->L; ++l) {
+        for (auto& p : h->last_pos[l]) p += delta;
+        h->last_entry[l] = -1;
+    }
+    h->delta_total += delta;
+    h->last_stream = s;
+    return RC_OK;
+}
+
+static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out, int n, void* stream,
+                         bool readtime) {
+    if (!h || !Q_bf16 || !out) return RC_ERR_ARG;
+    if (layer < 0 || layer >= h->L || n < 1) return RC_ERR_ARG;
+    if (h->last_n[layer] == 0 || n != h->last_n[layer] || h->occupancy[layer] == 0) return RC_ERR_STATE;
+    if (readtime && !h->ablation) return RC_ERR_STATE;
+    if (check_sticky() != RC_OK) return RC_ERR_CUDA;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int entry = h->last_entry[layer];
+    if (entry < 0 || !h->pool[entry].valid || h->pool[entry].n != n ||
+        h->pool[entry].p0 != h->last_pos[layer][0] ||
+        (!h->pool[entry].arith && h->pool[entry].pos != h->last_pos[layer])) {
+        int err = RC_OK;
+        entry = rope_entry(h, h->last_pos[layer].data(), n, s, &err);
+        if (entry < 0) return err;
+        h->last_entry[layer] = entry;
+    } else {
+        h->pool[entry].stamp = ++h->clock;
+    }
+    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D;
+    const size_t lsc = static_cast<size_t>(layer) * h->H * h->Cpad;
+    AttnParams ap{};
+    if (readtime) {
+        ReadtimeParams rp{};
+        const size_t raw = static_cast<size_t>(layer) * h->H * h->Cpad * h->D;
+        rp.kraw = h->d_kraw + raw;
+        rp.vraw = h->d_vraw + raw;
+        rp.slot_rope = h->d_slot_rope + static_cast<size_t>(layer) * h->Cpad * (h->D / 2);
+        rp.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
+        rp.kc = h->d_rt_kc;
+        rp.vt = h->d_rt_vt;
+        rp.sk = h->d_rt_sk;
+        rp.sv = h->d_rt_sv;
+        rp.H = h->H;
+        rp.C = h->C;
+        rp.T = h->T;
+        rp.Cpad = h->Cpad;
+        if (launch_readtime(rp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+        h->launches += 1;
+        ap.kc = h->d_rt_kc;
+        ap.vt = h->d_rt_vt;
+        ap.sk = h->d_rt_sk;
+        ap.sv = h->d_rt_sv;
+    } else {
+        ap.kc = h->d_kc + lring;
+        ap.vt = h->d_vt + lring;
+        ap.sk = h->d_sk + lsc;
+        ap.sv = h->d_sv + lsc;
+    }
+    ap.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
+    ap.q = static_cast<const __nv_bfloat16*>(Q_bf16);
+    ap.rope = h->pool[entry].d_table;
+    ap.out = out;
+    ap.n = n;
+    ap.H = h->H;
+    ap.C = h->C;
+    ap.T = h->T;
+    ap.Cpad = h->Cpad;
+    ap.masked = (h->occupancy[layer] < h->C) ? 1 : 0;
+    ap.sm_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+    ap.status = h->d_status;
+    if (launch_attention(ap, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    h->last_stream = s;
+    return RC_OK;
+}
+
+int rc_attend(rc_cache* h, int layer, const void* Q_bf16, float* out_f32, int n, void* stream) {
+    return attend_common(h, layer, Q_bf16, out_f32, n, stream, false);
+}
+
+int rc_attend_readtime(rc_cache* h, int layer, const void* Q_bf16, float* out_f32, int n, void* stream) {
+    return attend_common(h, layer, Q_bf16, out_f32, n, stream, true);
+}
+
+int rc_cache_sync(rc_cache* h) {
+    if (!h) return RC_ERR_ARG;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return RC_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RC_ERR_CUDA;
+    int st = 0;
+    if (cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+    if (st != 0) {
+        cudaMemset(h->d_status, 0, sizeof(int));
+        return RC_ERR_TIMEOUT;
+    }
+    return RC_OK;
+}
+
+static int export_ring(rc_cache* h, const uint8_t* d_kc, const uint8_t* d_vt, const float* d_sk, const float* d_sv,
+                       uint8_t* kcodes, float* kscale, uint8_t* vcodes, float* vscale) {
+    const int H = h->H, D = h->D, C = h->C, T = h->T, Cp = h->Cpad;
+    const size_t one = static_cast<size_t>(H) * T * kTileSlots * D;
+    std::vector<uint8_t> buf;
+    if (kcodes) {
+        buf.resize(one);
+        if (cudaMemcpy(buf.data(), d_kc, one, cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            for (int s = 0; s < C; ++s) {
+                const uint8_t* tile = buf.data() + (static_cast<size_t>(hh) * T + s / kTileSlots) * kTileSlots * D;
+                uint8_t* dst = kcodes + (static_cast<size_t>(hh) * C + s) * D;
+                for (int d = 0; d < D; ++d) dst[d] = tile[ktile_off(s % kTileSlots, d, D)];
+            }
+    }
+    if (vcodes) {
+        buf.resize(one);
+        if (cudaMemcpy(buf.data(), d_vt, one, cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            for (int s = 0; s < C; ++s) {
+                const uint8_t* tile = buf.data() + (static_cast<size_t>(hh) * T + s / kTileSlots) * kTileSlots * D;
+                uint8_t* dst = vcodes + (static_cast<size_t>(hh) * C + s) * D;
+                for (int d = 0; d < D; ++d) dst[d] = tile[vtile_off(d, s % kTileSlots)];
+            }
+    }
+    std::vector<float> sbuf;
+    if (kscale || vscale) sbuf.resize(static_cast<size_t>(H) * Cp);
+    if (kscale) {
+        if (cudaMemcpy(sbuf.data(), d_sk, sizeof(float) * sbuf.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            std::memcpy(kscale + static_cast<size_t>(hh) * C, sbuf.data() + static_cast<size_t>(hh) * Cp,
+                        sizeof(float) * C);
+    }
+    if (vscale) {
+        if (cudaMemcpy(sbuf.data(), d_sv, sizeof(float) * sbuf.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            std::memcpy(vscale + static_cast<size_t>(hh) * C, sbuf.data() + static_cast<size_t>(hh) * Cp,
+                        sizeof(float) * C);
+    }
+    return RC_OK;
+}
+
+int rc_cache_export(rc_cache* h, int layer, uint8_t* kcodes, float* kscale, uint8_t* vcodes, float* vscale,
+                    int64_t* pos, int64_t* gid) {
+    if (!h || layer < 0 || layer >= h->L) return RC_ERR_ARG;
+    int st = rc_cache_sync(h);
+    if (st != RC_OK) return st;
+    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D;
+    const size_t lsc = static_cast<size_t>(layer) * h->H * h->Cpad;
+    st = export_ring(h, h->d_kc + lring, h->d_vt + lring, h->d_sk + lsc, h->d_sv + lsc, kcodes, kscale, vcodes,
+                     vscale);
+    if (st != RC_OK) return st;
+    const size_t lb = static_cast<size_t>(layer) * h->C;
+    if (pos) std::memcpy(pos, h->pos.data() + lb, sizeof(int64_t) * h->C);
+    if (gid) std::memcpy(gid, h->gid.data() + lb, sizeof(int64_t) * h->C);
+    return RC_OK;
+}
+
+int rc_cache_export_readtime(rc_cache* h, uint8_t* kcodes, float* kscale, uint8_t* vcodes, float* vscale) {
+    if (!h) return RC_ERR_ARG;
+    if (!h->ablation) return RC_ERR_STATE;
+    int st = rc_cache_sync(h);
+    if (st != RC_OK) return st;
+    return export_ring(h, h->d_rt_kc, h->d_rt_vt, h->d_rt_sk, h->d_rt_sv, kcodes, kscale, vcodes, vscale);
+}
+
+int rc_cache_occupancy(const rc_cache* h, int layer) {
+    if (!h || layer < 0 || layer >= h->L) return RC_ERR_ARG;
+    return h->occupancy[layer];
+}
+
+int64_t rc_cache_delta_total(const rc_cache* h) { return h ? h->delta_total : 0; }
+
+int64_t rc_cache_launch_count(const rc_cache* h) { return h ? h->launches : 0; }
+
+}  // extern "C"

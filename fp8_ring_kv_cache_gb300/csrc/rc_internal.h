@@ -1,0 +1,98 @@
+// rc_internal.h -- kernel parameter blocks and launchers shared by the host
+// layer (rc_host.cu) and the kernel translation units.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace rc {
+
+constexpr int kMaxHalfDim = 64;  // head_dim <= 128
+
+// K1: cos/sin of p * theta_i for the n positions of one write, fp64 angle.
+struct RopeTableParams {
+    float2* table;         // [n][D/2] (cos, sin)
+    const int64_t* pos;    // device positions, or nullptr for p0 + t
+    int64_t p0;
+    const double* theta;   // [D/2] fp64 frequencies
+    int n;
+    int half;              // D/2
+};
+
+// K2: fused RoPE + per-head amax + E4M3 quantisation + scatter into ring slots.
+struct WriteParams {
+    uint8_t* kc;           // layer base [H][T][128][D]
+    uint8_t* vt;           // layer base [H][T][D][128]
+    float* sk;             // layer base [H][Cpad]
+    float* sv;
+    int32_t* grp;          // layer base [Cpad]
+    const __nv_bfloat16* K;  // [n][H][D]
+    const __nv_bfloat16* V;
+    const float2* rope;    // [n][D/2]
+    const int64_t* pos;    // device positions or nullptr
+    int64_t p0;
+    int64_t delta_total;
+    int n, H, C, T, Cpad;
+    int32_t group;         // compact write-group index of this write
+    __nv_bfloat16* kraw;   // read-time store [H][Cpad][D] (nullptr if off)
+    __nv_bfloat16* vraw;
+    float2* slot_rope;     // read-time store [Cpad][D/2] (nullptr if off)
+};
+
+// K3: in-place delta rotation with per-(layer, head, group) requantisation.
+struct RotateParams {
+    uint8_t* kc;           // all layers [L][H][T][128][D]
+    float* sk;             // [L][H][Cpad]
+    const int32_t* grp;    // [L][Cpad]
+    int H, C, T, Cpad;
+    float2 cs[kMaxHalfDim];  // (cos, sin) of delta * theta_i
+};
+
+// K5: read-time ablation, rebuild one layer's FP8 ring from the bf16 store
+// with one scale per head (and per K / V) over every occupied slot.
+struct ReadtimeParams {
+    const __nv_bfloat16* kraw;  // layer [H][Cpad][D]
+    const __nv_bfloat16* vraw;
+    const float2* slot_rope;    // layer [Cpad][D/2]
+    const int32_t* grp;         // layer [Cpad]
+    uint8_t* kc;                // scratch ring [H][T][128][D]
+    uint8_t* vt;                // [H][T][D][128]
+    float* sk;                  // [H][Cpad]
+    float* sv;
+    int H, C, T, Cpad;
+};
+
+// K4: FP8 attention over one layer's ring.
+struct AttnParams {
+    const uint8_t* kc;     // layer [H][T][128][D]
+    const uint8_t* vt;     // layer [H][T][D][128]
+    const float* sk;       // layer [H][Cpad]
+    const float* sv;
+    const int32_t* grp;    // layer [Cpad]
+    const __nv_bfloat16* q;  // [n][H][D]
+    const float2* rope;    // [n][D/2]
+    float* out;            // [n][H][D]
+    int n, H, C, T, Cpad;
+    int masked;            // 1: some slots are empty, read grp
+    float sm_log2;         // log2(e) / sqrt(D)
+    int* status;           // device status word
+};
+
+cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t s);
+cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s);
+cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status);
+cudaError_t launch_readtime(const ReadtimeParams& p, int D, cudaStream_t s);
+cudaError_t launch_attention(const AttnParams& p, int D, cudaStream_t s);
+
+// Status values a kernel writes into the device status word.
+enum DeviceStatus : int {
+    kDevOk = 0,
+    kDevTimeoutLoader = 101,
+    kDevTimeoutMma = 102,
+    kDevTimeoutSoftmax = 103,
+    kDevTimeoutConvert = 104,
+    kDevTimeoutEpilogue = 105,
+};
+
+}  // namespace rc

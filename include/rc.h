@@ -1,0 +1,182 @@
+/*
+ * rc.h -- C ABI of the write-time FP8 ring KV cache for one GB300 (sm_103a).
+ *
+ * The operations come from the pages about "Runway Characters: Serving a 57B
+ * Video Diffusion Transformer for Real-Time Conversation" (arXiv 2611.05642):
+ *   - paperdot abstract mirror: "a ring cache, RoPE and FP8 quantization
+ *     applied once per write, and a delta rotation when positions reset";
+ *     each chunk makes 240 attention calls that read a 5,788-slot cache in
+ *     which 757 tokens are new.
+ *   - cpdf.ai blog, section "Como rodar 57B em tempo real com batch size 1":
+ *     rotary positions and FP8 quantisation move from read time to write
+ *     time, and the ring advances the window without copies.
+ *   - cpdf.ai blog, section "Blackwell, escalabilidade e limites do
+ *     decodificador": the FP8 attention kernel uses per-head scales.
+ *
+ * Conventions shared by every call:
+ *   - Status: 0 (RC_OK) or a negative RC_ERR_* code.  Argument and state
+ *     errors are found on the host before anything is launched, and leave the
+ *     cache unchanged.  Errors of kernels already launched surface as
+ *     RC_ERR_CUDA from a later call, or from rc_cache_sync.  No C++ exception
+ *     crosses this boundary.
+ *   - Device pointers are plain CUDA device addresses (for example a torch
+ *     tensor's data_ptr()).  The caller keeps them alive until the work on
+ *     `stream` that reads or writes them has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls on one handle must be issued on one stream, or ordered
+ *     by the caller; a handle is not thread-safe.
+ *   - Memory: rc_cache_create allocates every device and pinned host buffer
+ *     the handle will ever use.  No later call allocates, for any write size
+ *     up to max_write.
+ *   - Layouts: K, V and Q are bf16, token-major [n][heads][head_dim] with
+ *     head_dim contiguous.  The attention output is fp32 with the same layout.
+ *     head_dim is 64 or 128.
+ */
+#ifndef RC_H
+#define RC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define RC_OK 0
+#define RC_ERR_ARG (-1)         /* bad argument: null pointer, size or index out of range,
+                                   two tokens of one write on the same slot */
+#define RC_ERR_STATE (-2)       /* call not valid in the current state: attention on a
+                                   layer never written, or query count different from
+                                   that layer's last write */
+#define RC_ERR_CUDA (-3)        /* a CUDA runtime call or a launched kernel failed */
+#define RC_ERR_OOM (-4)         /* rc_cache_create could not allocate */
+#define RC_ERR_TIMEOUT (-5)     /* a kernel gave up a bounded wait and returned early;
+                                   its output is not valid */
+#define RC_ERR_UNSUPPORTED (-6) /* shape not supported (head_dim other than 64 or 128,
+                                   or a device that is not sm_103) */
+
+/* ---- configuration ------------------------------------------------------ */
+/* Keep the unrotated bf16 K, V of every slot as well, so that rc_attend_readtime
+   can redo RoPE and quantisation of the whole cache at read time. */
+#define RC_F_READTIME_ABLATION 1u
+
+typedef struct rc_config {
+    int layers;       /* attention layers with one ring each (>= 1) */
+    int heads;        /* heads per layer (>= 1) */
+    int head_dim;     /* 64 or 128 */
+    int slots;        /* ring capacity C per layer (>= 1) */
+    int max_write;    /* largest n of one write (1 .. slots) */
+    double rope_base; /* RoPE base; theta_i = base^(-2i/head_dim) (> 1) */
+    unsigned flags;   /* RC_F_* */
+} rc_config;
+
+typedef struct rc_cache rc_cache; /* opaque; owns all of its memory */
+
+/*
+ * Create a cache on CUDA device `device` and store the handle in *out.
+ * Every slot starts empty.  Allocates the FP8 rings (2 * layers * heads *
+ * ceil(slots/128)*128 * head_dim bytes), the per-slot scales, the RoPE table
+ * pool and the pinned position staging, and with RC_F_READTIME_ABLATION the
+ * bf16 store.  On error *out is NULL and nothing is leaked.
+ */
+int rc_cache_create(const rc_config *cfg, int device, rc_cache **out);
+
+/*
+ * Write n new tokens into ring `layer` (paperdot abstract: "RoPE and FP8
+ * quantization applied once per write").  K_bf16 and V_bf16 are device
+ * pointers to [n][heads][head_dim] bf16.  positions is a HOST array of n
+ * int64 token positions (any sign).  Token t goes to slot
+ * floormod(positions[t] - delta_total, slots), replacing what was there.
+ * For every head, K is rotated by RoPE at its position; then K and V each get
+ * one fp32 scale s = fl32(amax/448) over the n tokens of that head (s = 1 if
+ * amax = 0), and each element is stored as the E4M3 code of fl32(x/s),
+ * rounded to nearest even and saturated to +-448.
+ * Errors: RC_ERR_ARG if layer is out of range, n < 1 or n > max_write, a
+ * pointer is NULL, or two tokens map to one slot.
+ * A position vector that is not an arithmetic run p0, p0+1, ... is copied to
+ * the device through pinned staging; an arithmetic run needs no copy.
+ */
+int rc_cache_write(rc_cache *h, int layer, const void *K_bf16, const void *V_bf16,
+                   const int64_t *positions, int n, void *stream);
+
+/*
+ * Position reset (paperdot abstract: "a delta rotation when positions
+ * reset").  Every occupied slot of every layer moves from position p to
+ * p + delta without moving slots: the stored keys are dequantised, rotated
+ * by delta, and each (layer, head, write group) is requantised in place with
+ * a fresh scale from its new amax.  Values are untouched.  The layers' last
+ * write positions move by delta too.  delta = 0 is a no-op.
+ */
+int rc_cache_delta_rotate(rc_cache *h, int64_t delta, void *stream);
+
+/*
+ * Attention call (paperdot abstract: the new tokens' queries read the whole
+ * cache).  Q_bf16 is a device pointer to [n][heads][head_dim] bf16 queries of
+ * the layer's last write; each is rotated at that token's (current) position.
+ * out_f32 is a device pointer to [n][heads][head_dim] fp32:
+ *   out = softmax(q . k_j / sqrt(head_dim)) over the occupied slots j, times v_j,
+ * with k_j, v_j the stored codes times their slot's scale.  No mask.
+ * Errors: RC_ERR_STATE if the layer was never written or n differs from the
+ * layer's last write; RC_ERR_ARG for NULL pointers or a bad layer.
+ */
+int rc_attend(rc_cache *h, int layer, const void *Q_bf16, float *out_f32, int n,
+              void *stream);
+
+/*
+ * Read-time ablation of rc_attend (the original design the pages describe
+ * in the abstract and in the cpdf.ai section "Como rodar 57B em tempo real
+ * com batch size 1": RoPE and FP8 quantisation of the WHOLE cache redone in
+ * every attention call).  Rebuilds this layer's FP8 ring from the unrotated
+ * bf16 store into a scratch ring, then runs the same attention kernel on it.
+ * Requires RC_F_READTIME_ABLATION, else RC_ERR_STATE.  The result equals
+ * rc_attend's as long as no delta rotation has requantised the write-time
+ * ring.
+ */
+int rc_attend_readtime(rc_cache *h, int layer, const void *Q_bf16, float *out_f32,
+                       int n, void *stream);
+
+/* Free everything the handle owns (waits for its device work first). NULL is ignored. */
+void rc_cache_destroy(rc_cache *h);
+
+/* A static description of a status code. */
+const char *rc_status_string(int status);
+
+/* ---- inspection and test support -------------------------------------- */
+
+/* Synchronise the handle's last stream and report any kernel error or timeout. */
+int rc_cache_sync(rc_cache *h);
+
+/*
+ * Copy ring `layer` to HOST buffers in canonical layout (synchronous):
+ * kcodes, vcodes: uint8 [heads][slots][head_dim] E4M3 codes; kscale, vscale:
+ * fp32 [heads][slots]; pos: int64 [slots] position (INT64_MIN = empty);
+ * gid: int64 [slots] serial number of the write that filled the slot
+ * (INT64_MIN = empty; writes are numbered 0, 1, ... per handle).  Any
+ * pointer may be NULL to skip that table.
+ */
+int rc_cache_export(rc_cache *h, int layer, uint8_t *kcodes, float *kscale,
+                    uint8_t *vcodes, float *vscale, int64_t *pos, int64_t *gid);
+
+/*
+ * Copy the scratch ring that the last rc_attend_readtime call built (same
+ * canonical layouts as rc_cache_export; synchronous).  RC_ERR_STATE without
+ * RC_F_READTIME_ABLATION.
+ */
+int rc_cache_export_readtime(rc_cache *h, uint8_t *kcodes, float *kscale,
+                             uint8_t *vcodes, float *vscale);
+
+/* Number of occupied slots of `layer`, or a negative status. */
+int rc_cache_occupancy(const rc_cache *h, int layer);
+
+/* Sum of all deltas applied so far. */
+int64_t rc_cache_delta_total(const rc_cache *h);
+
+/* Number of kernel launches this handle has made (for launch accounting). */
+int64_t rc_cache_launch_count(const rc_cache *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RC_H */

@@ -83,6 +83,8 @@ def _load():
         lib.orc_attend.restype = i32
         lib.orc_attend_image.argtypes = [i32, i32, i32, f64, P, P, P, P, P, P, P, i32, P]
         lib.orc_attend_image.restype = i32
+        lib.orc_readtime_image.argtypes = [i32, i32, i32, f64, P, P, P, P, P, P, P]
+        lib.orc_readtime_image.restype = None
         lib.orc_export.argtypes = [P, i32, P, P, P, P, P, P]
         lib.orc_export.restype = None
         lib.orc_import.argtypes = [P, i32, P, P, P, P, P, P, P, i32]
@@ -180,6 +182,21 @@ def attend_image(kc, sk, vc, sv, pos, Q, qpos, base: float = 10000.0) -> np.ndar
     if m < 0:
         raise ValueError("attention over an empty cache")
     return out
+
+
+def readtime_image(kraw, vraw, pos, base: float = 10000.0) -> dict:
+    """Read-time quantisation of a whole layer: one scale per head over every occupied slot.
+
+    kraw, vraw: bf16 [H][C][d] (the unrotated rows of every slot); pos: int64 [C].
+    """
+    kb, vb = _bf16_bits(kraw), _bf16_bits(vraw)
+    pos = np.ascontiguousarray(pos, dtype=np.int64)
+    H, C, d = kb.shape
+    st = dict(kcodes=np.zeros((H, C, d), np.uint8), kscale=np.zeros((H, C), np.float32),
+              vcodes=np.zeros((H, C, d), np.uint8), vscale=np.zeros((H, C), np.float32))
+    _load().orc_readtime_image(H, d, C, base, _ptr(kb), _ptr(vb), _ptr(pos), _ptr(st["kcodes"]),
+                               _ptr(st["kscale"]), _ptr(st["vcodes"]), _ptr(st["vscale"]))
+    return st
 
 
 # ------------------------------------------------------------------ state machine

@@ -476,3 +476,51 @@ void orc_last_pos(const orc_cache *c, int l, int64_t *out)
 {
     memcpy(out, c->last_pos + (size_t)l * c->C, sizeof(int64_t) * c->last_n[l]);
 }
+
+/*
+ * Read-time quantisation of one layer (the original design the pages describe:
+ * RoPE and FP8 quantisation of the whole cache in every call).  kraw, vraw are
+ * the unrotated bf16 rows of every slot ([H][C][d] bits), pos[C] their
+ * positions (ORC_EMPTY = free).  One scale per head for K and one for V over
+ * all occupied slots; codes of free slots are 0 with scale 0.
+ */
+void orc_readtime_image(int H, int d, int C, double base, const uint16_t *kraw,
+                        const uint16_t *vraw, const int64_t *pos,
+                        uint8_t *kc, float *sk, uint8_t *vc, float *sv)
+{
+    double *xk = (double *)malloc(sizeof(double) * (size_t)C * d);
+    double *xv = (double *)malloc(sizeof(double) * (size_t)C * d);
+    int *occ = (int *)malloc(sizeof(int) * (size_t)C);
+    for (int h = 0; h < H; ++h) {
+        size_t m = 0;
+        for (int s = 0; s < C; ++s) {
+            if (pos[s] == ORC_EMPTY) continue;
+            occ[m] = s;
+            for (int i = 0; i < d; ++i) {
+                size_t src = ((size_t)h * C + s) * d + i;
+                xk[m * d + i] = orc_bf16_to_double(kraw[src]);
+                xv[m * d + i] = orc_bf16_to_double(vraw[src]);
+            }
+            orc_rope_rotate(xk + m * d, d, pos[s], base);
+            ++m;
+        }
+        uint8_t *ck = (uint8_t *)malloc(m * (size_t)d + 1);
+        uint8_t *cv = (uint8_t *)malloc(m * (size_t)d + 1);
+        float fk = quantise_group(xk, m, d, ck);
+        float fv = quantise_group(xv, m, d, cv);
+        memset(kc + (size_t)h * C * d, 0, (size_t)C * d);
+        memset(vc + (size_t)h * C * d, 0, (size_t)C * d);
+        for (int s = 0; s < C; ++s) {
+            sk[(size_t)h * C + s] = 0.0f;
+            sv[(size_t)h * C + s] = 0.0f;
+        }
+        for (size_t j = 0; j < m; ++j) {
+            memcpy(kc + ((size_t)h * C + occ[j]) * d, ck + j * d, d);
+            memcpy(vc + ((size_t)h * C + occ[j]) * d, cv + j * d, d);
+            sk[(size_t)h * C + occ[j]] = fk;
+            sv[(size_t)h * C + occ[j]] = fv;
+        }
+        free(ck); free(cv);
+    }
+    free(xk); free(xv); free(occ);
+}

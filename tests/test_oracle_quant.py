@@ -106,3 +106,39 @@ def test_delta_rotation_requantises_groups(oracle_mod):
         exact = oracle_mod.rope_rows(K[:, h, :].to(torch.float64).numpy(), pos - 12345)
         err = np.abs(dq[h] - exact).max() / np.abs(exact).max()
         assert err < 2 * 2.0 ** -4   # two E4M3 roundings, each <= half a step (relative 2^-4)
+
+
+def test_readtime_image_matches_write_time_when_one_group(oracle_mod):
+    # a cache filled by ONE write: the read-time image (one scale per head over
+    # the whole cache) equals the write-time state exactly
+    H, d, C = 3, 16, 40
+    K, V = si.normal_bf16(C, H, d, 41), si.normal_bf16(C, H, d, 42)
+    pos = np.arange(500, 500 + C)
+    oc = oracle_mod.OracleCache(1, H, d, C)
+    oc.write(0, K, V, pos)
+    st = oc.export(0)
+    slots = np.array([oc.slot_of(p) for p in pos])
+    kraw = torch.zeros(H, C, d, dtype=torch.bfloat16)
+    vraw = torch.zeros(H, C, d, dtype=torch.bfloat16)
+    kraw[:, slots] = K.permute(1, 0, 2)
+    vraw[:, slots] = V.permute(1, 0, 2)
+    img = oracle_mod.readtime_image(kraw, vraw, st["pos"])
+    for k in ("kcodes", "kscale", "vcodes", "vscale"):
+        assert np.array_equal(img[k], st[k]), k
+
+
+def test_readtime_image_whole_cache_scale(oracle_mod):
+    # two writes with very different magnitudes: read time uses one scale per head
+    H, d, C = 2, 8, 20
+    oc = oracle_mod.OracleCache(1, H, d, C)
+    K1 = si.normal_bf16(10, H, d, 1, mult=torch.full((H, 1), 10.0))
+    K2 = si.normal_bf16(10, H, d, 2)
+    oc.write(0, K1, K1, np.arange(10))
+    oc.write(0, K2, K2, np.arange(10, 20))
+    st = oc.export(0)
+    assert st["kscale"][0, 0] != st["kscale"][0, 15]
+    kraw = torch.cat([K1, K2]).permute(1, 0, 2).contiguous()
+    img = oracle_mod.readtime_image(kraw, kraw, st["pos"])
+    assert len(np.unique(img["kscale"][0])) == 1
+    x = oracle_mod.rope_rows(kraw[0].to(torch.float64).numpy(), st["pos"])
+    assert abs(img["kscale"][0, 0] - np.abs(x).max() / 448) <= 1e-6 * np.abs(x).max() / 448
