@@ -443,8 +443,50 @@ def run_reference(args, rank: int, world: int) -> dict | None:
     }
 
 
+def run_profile_case(kind: str) -> None:
+    """Small fixed cases for ncu captures (a few hundred MB on the device).
+
+    attention : 2 layers of the production ring (48 x 128, 5,788 slots full);
+                3 attention calls alternate between the layers.
+    write     : 3 writes of 757 tokens into 3 layers.
+    rotate    : 2 delta rotations of 4 full layers.
+    """
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+    import synth_inputs as si
+
+    nl = {"attention": 2, "write": 3, "rotate": 4}[kind]
+    cache = rc.RingKVCache(nl, H, D, C, max_write=C)
+    mult = si.outlier_mask(H, D, 11)
+    kp = si.normal_bf16(PREFILL, H, D, 1, "cuda", mult)
+    vp = si.normal_bf16(PREFILL, H, D, 2, "cuda", mult)
+    kn = si.normal_bf16(N_NEW, H, D, 3, "cuda", mult)
+    vn = si.normal_bf16(N_NEW, H, D, 4, "cuda", mult)
+    q = si.normal_bf16(N_NEW, H, D, 5, "cuda")
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device="cuda")
+    for layer in range(nl):
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+        cache.write(layer, kn, vn, np.arange(PREFILL, C))
+    cache.sync()
+    if kind == "attention":
+        for i in range(3):
+            cache.attend(i % nl, q, out)
+    elif kind == "write":
+        for layer in range(nl):
+            cache.write(layer, kn, vn, np.arange(PREFILL, C))
+    else:
+        for _ in range(2):
+            cache.delta_rotate(-N_NEW)
+    cache.sync()
+    print(f"profile case {kind} done, {cache.launch_count} launches")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", choices=["attention", "write", "rotate"], default=None,
+                    help="run a small fixed case for an ncu capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -452,6 +494,9 @@ def main():
     ap.add_argument("--cpu-calls", type=int, default=3, help="oracle calls timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
