@@ -39,6 +39,12 @@ class rc_config(ctypes.Structure):
                 ("flags", ctypes.c_uint)]
 
 
+class rc_ring_view(ctypes.Structure):
+    _fields_ = [("kcodes", ctypes.c_void_p), ("vcodes", ctypes.c_void_p), ("kscale", ctypes.c_void_p),
+                ("vscale", ctypes.c_void_p), ("group", ctypes.c_void_p), ("heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("slots", ctypes.c_int)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -59,6 +65,8 @@ def _load() -> ctypes.CDLL:
         "rc_cache_occupancy": ([P, I], I),
         "rc_cache_delta_total": ([P], I64),
         "rc_cache_launch_count": ([P], I64),
+        "rc_ring_write_noalloc": ([ctypes.POINTER(rc_ring_view), P, P, P, I, I64, ctypes.c_int32,
+                                   ctypes.c_double, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -241,3 +249,31 @@ class RingKVCache:
     @property
     def launch_count(self):
         return rc_cache_launch_count(self.handle)
+
+
+RC_NOALLOC_MAX_TOKENS = 4096
+
+
+def rc_ring_write_noalloc(ring: dict, K, V, positions, delta_total: int, group: int,
+                          rope_base: float = 10000.0, stream=None) -> None:
+    """Write into caller-owned ring tensors without any device allocation.
+
+    ring: dict of torch CUDA tensors kcodes, vcodes (uint8), kscale, vscale
+    (float32), group (int32) laid out as include/rc.h describes, plus ints
+    heads, head_dim, slots."""
+    import torch
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    n = int(pos.shape[0])
+    H, Dh, C = int(ring["heads"]), int(ring["head_dim"]), int(ring["slots"])
+    T = (C + 127) // 128
+    view = rc_ring_view(
+        _dev_ptr(ring["kcodes"], torch.uint8, (H * T * 128 * Dh,), "kcodes").value,
+        _dev_ptr(ring["vcodes"], torch.uint8, (H * T * 128 * Dh,), "vcodes").value,
+        _dev_ptr(ring["kscale"], torch.float32, (H * T * 128,), "kscale").value,
+        _dev_ptr(ring["vscale"], torch.float32, (H * T * 128,), "vscale").value,
+        _dev_ptr(ring["group"], torch.int32, (T * 128,), "group").value, H, Dh, C)
+    kp = _dev_ptr(K, torch.bfloat16, (n, H, Dh), "K")
+    vp = _dev_ptr(V, torch.bfloat16, (n, H, Dh), "V")
+    _check(lib.rc_ring_write_noalloc(ctypes.byref(view), kp, vp, pos.ctypes.data_as(ctypes.c_void_p), n,
+                                     int(delta_total), int(group), float(rope_base), _stream_ptr(stream)),
+           "rc_ring_write_noalloc")

@@ -166,6 +166,65 @@ int rc_cache_export(rc_cache *h, int layer, uint8_t *kcodes, float *kscale,
 int rc_cache_export_readtime(rc_cache *h, uint8_t *kcodes, float *kscale,
                              uint8_t *vcodes, float *vscale);
 
+/* ---- allocation-free write into a caller-owned ring -------------------- */
+/*
+ * No counterpart in the paper: this is an integration convenience.
+ *
+ * Some callers cannot call cudaMalloc: a process whose device memory is all
+ * reserved up front by another allocator (a framework's caching allocator or
+ * a fixed arena), where a new allocation would fail or fragment that pool; or
+ * a latency-critical loop that must never pay for cudaMalloc / cudaFree, which
+ * can synchronise the whole device.  rc_ring_write_noalloc serves them: it
+ * performs exactly the write of rc_cache_write (RoPE table kernel, then the
+ * fused RoPE + per-head amax + E4M3 write kernel) into ring buffers that the
+ * CALLER owns, and it allocates nothing.  Its only scratch -- the RoPE
+ * frequencies, a copy of non-arithmetic positions and the per-token cos/sin
+ * table -- lives in one file-scope __device__ array of about 2 MiB
+ * (RC_NOALLOC_MAX_TOKENS tokens x 64 pairs x 8 bytes, plus 33 KiB), which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Rules:
+ *   - n <= RC_NOALLOC_MAX_TOKENS, else RC_ERR_ARG (nothing is launched).
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents.  Calls that overlap on the GPU (other streams or
+ *     threads without ordering) race on it; order them on one stream.
+ *   - positions is a HOST array; a non-arithmetic run is copied into the
+ *     array from pageable memory (the call returns once it is staged).
+ *   - The caller keeps the ring state: delta_total (the sum of resets applied
+ *     to this ring) and a write-group index in [0, slots) unique among the
+ *     ring's live groups.  There is no delta rotation or attention entry on a
+ *     caller-owned ring; this is the write alone.
+ *
+ * Ring layout (T = ceil(slots / 128) tiles per head, Cpad = 128 T), all device
+ * memory the caller allocated:
+ *   kcodes [heads][T][128][head_dim] E4M3: slot s is row s % 128 of tile
+ *          s / 128; byte d of a row sits at 16-byte chunk (d / 16) XOR x,
+ *          x = row % 8 (head_dim 128) or (row / 2) % 4 (head_dim 64).
+ *   vcodes [heads][T][head_dim][128] E4M3 (transposed): element (d, s) sits in
+ *          row d of tile s / 128 at chunk ((s % 128) / 16) XOR (d % 8).
+ *   kscale, vscale [heads][Cpad] fp32: the scale of each slot's write group.
+ *   group  [Cpad] int32: the slot's write-group index (-1 = empty).
+ */
+#define RC_NOALLOC_MAX_TOKENS 4096
+
+typedef struct rc_ring_view {
+    uint8_t *kcodes;  /* device, see the layout above */
+    uint8_t *vcodes;
+    float *kscale;
+    float *vscale;
+    int32_t *group;
+    int heads;        /* >= 1 */
+    int head_dim;     /* 64 or 128 */
+    int slots;        /* ring capacity C >= 1 */
+} rc_ring_view;
+
+int rc_ring_write_noalloc(const rc_ring_view *ring, const void *K_bf16, const void *V_bf16,
+                          const int64_t *positions, int n, int64_t delta_total,
+                          int32_t group, double rope_base, void *stream);
+
 /* Number of occupied slots of `layer`, or a negative status. */
 int rc_cache_occupancy(const rc_cache *h, int layer);
 

@@ -1,0 +1,104 @@
+"""rc_ring_write_noalloc against rc_cache_write, through the C ABI.
+
+Some callers cannot call cudaMalloc: a process whose device memory is all
+reserved by another allocator (a framework's caching allocator or a fixed
+arena), or a latency-critical loop that must never pay for cudaMalloc/cudaFree,
+which can synchronise the device.  rc_ring_write_noalloc writes into a ring the
+caller owns and keeps its only scratch (the RoPE table) in a static device
+array.  Here the test itself allocates that caller-owned ring with torch, makes
+two writes in a row with both entry points on the same inputs, and compares
+codes, scales and groups with the tolerances of the other parity tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+from parity_util import check_codes, check_scales
+
+pytestmark = pytest.mark.gpu
+
+
+def _koff(row, col, D):
+    x = (row & 7) if D == 128 else ((row >> 1) & 3)
+    return row * D + ((((col >> 4) ^ x) << 4) | (col & 15))
+
+
+def _voff(drow, slot):
+    return drow * 128 + ((((slot >> 4) ^ (drow & 7)) << 4) | (slot & 15))
+
+
+def _canonical(ring, H, D, C):
+    """Caller-owned ring buffers -> [H][C][D] codes and [H][C] scales (the layout rc.h documents)."""
+    T = (C + 127) // 128
+    kc = ring["kcodes"].cpu().numpy().reshape(H, T, 128 * D)
+    vc = ring["vcodes"].cpu().numpy().reshape(H, T, 128 * D)
+    s = np.arange(C)
+    d = np.arange(D)
+    kidx = _koff((s % 128)[:, None], d[None, :], D)           # [C][D]
+    vidx = _voff(d[None, :], (s % 128)[:, None])              # [C][D]
+    tiles = (s // 128)[:, None]
+    out = dict(kcodes=kc[:, tiles, kidx], vcodes=vc[:, tiles, vidx],
+               kscale=ring["kscale"].cpu().numpy().reshape(H, T * 128)[:, :C],
+               vscale=ring["vscale"].cpu().numpy().reshape(H, T * 128)[:, :C],
+               group=ring["group"].cpu().numpy()[:C])
+    return out
+
+
+def _new_ring(H, D, C):
+    T = (C + 127) // 128
+    return dict(kcodes=torch.zeros(H * T * 128 * D, dtype=torch.uint8, device="cuda"),
+                vcodes=torch.zeros(H * T * 128 * D, dtype=torch.uint8, device="cuda"),
+                kscale=torch.zeros(H * T * 128, dtype=torch.float32, device="cuda"),
+                vscale=torch.zeros(H * T * 128, dtype=torch.float32, device="cuda"),
+                group=torch.full((T * 128,), -1, dtype=torch.int32, device="cuda"),
+                heads=H, head_dim=D, slots=C)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_noalloc_write_matches_cache_write(D):
+    import fp8_ring_kv_cache_gb300 as rc
+    from fp8_ring_kv_cache_gb300._binding import rc_ring_write_noalloc
+
+    H, C = 8, 1000
+    cache = rc.RingKVCache(1, H, D, C)
+    ring = _new_ring(H, D, C)
+    writes = [(0, 600, 0.5), (600, 500, 3.0)]   # the second write wraps onto slots 0..99
+    inputs = []
+    for i, (p0, n, scale) in enumerate(writes):
+        k = si.normal_bf16(n, H, D, 9100 + i, "cuda", mult=torch.full((H, 1), scale))
+        v = si.normal_bf16(n, H, D, 9200 + i, "cuda")
+        inputs.append((k, v, np.arange(p0, p0 + n)))
+    torch.cuda.synchronize()
+    for i, (k, v, pos) in enumerate(inputs):
+        cache.write(0, k, v, pos)
+        free_before = torch.cuda.mem_get_info()[0]
+        rc_ring_write_noalloc(ring, k, v, pos, delta_total=0, group=i)
+        torch.cuda.synchronize()
+        if i > 0:
+            # after the first call's one-time set-up, a call takes no device memory
+            assert torch.cuda.mem_get_info()[0] == free_before
+        want = cache.export(0)
+        got = _canonical(ring, H, D, C)
+        occ = want["pos"] != rc.EMPTY
+        check_codes(got["kcodes"][:, occ], want["kcodes"][:, occ], f"write {i} K codes")
+        check_codes(got["vcodes"][:, occ], want["vcodes"][:, occ], f"write {i} V codes")
+        check_scales(got["kscale"][:, occ], want["kscale"][:, occ], f"write {i} K scales")
+        check_scales(got["vscale"][:, occ], want["vscale"][:, occ], f"write {i} V scales")
+        # the slots of write j carry group j; untouched slots stay empty
+        assert np.array_equal(got["group"][occ], want["gid"][occ].astype(np.int32))
+        assert (got["group"][~occ] == -1).all()
+    cache.close()
+
+
+def test_noalloc_rejects_oversize():
+    import fp8_ring_kv_cache_gb300 as rc
+    from fp8_ring_kv_cache_gb300._binding import RC_NOALLOC_MAX_TOKENS, rc_ring_write_noalloc
+
+    H, D, C = 2, 64, RC_NOALLOC_MAX_TOKENS + 8
+    ring = _new_ring(H, D, C)
+    n = RC_NOALLOC_MAX_TOKENS + 1
+    k = torch.zeros(n, H, D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rc.RcError) as e:
+        rc_ring_write_noalloc(ring, k, k, np.arange(n), delta_total=0, group=0)
+    assert e.value.status == rc.RC_ERR_ARG
