@@ -1,26 +1,33 @@
-// rc_attention.cu -- K4, the attention call over the FP8 ring (paperdot
-// abstract: the 757 new tokens' queries read all 5,788 slots, 240 calls per
-// chunk; cpdf.ai "Blackwell, escalabilidade e limites do decodificador": the
-// FP8 attention kernel with per-head scales that the B200 build lacked).
+// rc_attention.cu -- the attention call over the FP8 ring (paperdot abstract:
+// the 757 new tokens' queries read all 5,788 slots, 240 calls per chunk;
+// cpdf.ai "Blackwell, escalabilidade e limites do decodificador": the FP8
+// attention kernel with per-head scales that the B200 build lacked).
 //
-// One CTA = one head x 256 query rows (two 128-row M tiles), 448 threads:
-//   warp 0        loader: one bulk copy per K tile, Vt tile and scale vectors
-//                 per 128-slot KV tile, double-buffered (mbarrier + complete_tx)
+// K6 q_prep_kernel: one warp per (query row, head): RoPE at the row's position,
+//    one fp32 scale sq = fl32(amax / 448) per row, and three E4M3 pieces
+//    (hi + mid + lo, 12 significant bits) of q / sq, written straight into the
+//    swizzled shared-memory image the attention kernel's A operand needs.
+//    Extra blocks take each head's largest V scale.
+// K4 attn_kernel: one CTA = one head x 256 query rows (two 128-row M tiles),
+//    448 threads:
+//   warp 0        loader: bulk copies of the prepared query pieces, then one
+//                 bulk copy per K tile, Vt tile and scale vectors per 128-slot
+//                 KV tile, double-buffered (mbarrier + complete_tx)
 //   warp 1        MMA issuer (one lane) and TMEM owner (512 columns)
 //   warps 2..5    softmax group 0 (rows 0..127; one row per thread / TMEM lane)
 //   warps 6..9    softmax group 1 (rows 128..255)
 //   warps 10..13  converter: Vt E4M3 tile -> fp16 tile (exact), 128-byte swizzle
 // Per KV tile j and M tile i:
-//   S_i = Q_i K_j^T on tcgen05 kind::f8f6f4: Q is split into three E4M3 pieces
-//         (hi + mid + lo, 12 significant bits) that accumulate into one fp32
-//         TMEM tile, so the score error stays inside the tolerance with FP8 K.
+//   S_i = Q_i K_j^T on tcgen05 kind::f8f6f4: the three Q pieces accumulate into
+//         one fp32 TMEM tile, so the score error stays inside the tolerance.
 //   softmax: score = S * sq_row * sk_slot * log2(e)/sqrt(D); online max and sum
-//         in registers; P = exp2(score - max) * sv_slot / max(sv) -> fp16,
-//         written back over S in TMEM.
+//         in registers (packed fp32x2 arithmetic, lazy rescaling of O);
+//         P = exp2(score - max) * sv_slot / max(sv) -> fp16, written back over
+//         S in TMEM.
 //   O_i += P_i V_j on tcgen05 kind::f16 with P read from TMEM (A operand) and
 //         the converted V tile from shared memory (B operand).
 // Two M tiles ping-pong so the tensor pipe works on one tile while the other
-// is in softmax.  Output: out = O * max(sv) / l, fp32.
+// is in softmax.  Output: out = O / sum(P''), fp32.
 #include "rc_device.cuh"
 #include "rc_internal.h"
 
@@ -34,6 +41,9 @@ constexpr int kMTile = 128;
 constexpr int kRowsPerCta = 2 * kMTile;
 constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpSm0 = 2, kWarpCvt = 10;
 constexpr uint32_t kTmemCols = 512;
+// The converted V tile holds code / 256 (the E4M3 bits placed in an fp16), so
+// O accumulates P V / 256; the epilogue multiplies the 256 back in.
+constexpr float kV16Scale = 256.f;
 
 // barrier indices
 enum : int {
@@ -45,7 +55,8 @@ enum : int {
     B_P_FULL = 8,    // [2]
     B_O_DONE = 10,   // [2]
     B_DRAIN = 12,
-    B_COUNT = 13
+    B_Q_FULL = 13,
+    B_COUNT = 14
 };
 
 template <int D>
@@ -57,16 +68,121 @@ struct AttnLayout {
     static constexpr uint32_t kStageBytes = ((2 * kTile + 3 * 512) + 1023) / 1024 * 1024;
     static constexpr uint32_t kV16 = kStage0 + kStages * kStageBytes;  // [2 halves][D][128 B] fp16
     static constexpr uint32_t kV16Bytes = 2 * D * 128;
-    static constexpr uint32_t kBar = kV16 + kV16Bytes;
+    static constexpr uint32_t kSq = kV16 + kV16Bytes;  // fp32 [256] row scales, then svmax (16 B)
+    static constexpr uint32_t kBar = kSq + 2 * kMTile * 4 + 16;
     static constexpr uint32_t kMisc = kBar + 8 * 16;
     static constexpr uint32_t kTotal = kMisc + 64;
     static constexpr uint32_t kAlloc = kTotal + 1024;  // room to align the base to 1024
 };
 
+// ---------------------------------------------------------------- K6 query preparation
+
+constexpr int kPrepWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kPrepWarps * 32) q_prep_kernel(QPrepParams p) {
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int rows = p.nmt * kMTile;
+    const int nrb = (p.H * rows + kPrepWarps - 1) / kPrepWarps;
+    if (static_cast<int>(blockIdx.x) >= nrb) {
+        // the head's largest V scale (empty slots hold 0)
+        const int h = blockIdx.x - nrb;
+        float m = 0.f;
+        for (int i = threadIdx.x; i < p.C; i += kPrepWarps * 32) m = fmaxf(m, p.sv[static_cast<size_t>(h) * p.Cpad + i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __shared__ float red[kPrepWarps];
+        if (lane == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float mm = 0.f;
+            for (int w = 0; w < kPrepWarps; ++w) mm = fmaxf(mm, red[w]);
+            p.svm[h * 4] = mm;
+        }
+        return;
+    }
+    const int w = blockIdx.x * kPrepWarps + (threadIdx.x >> 5);
+    if (w >= p.H * rows) return;
+    const int h = w / rows, row = w - h * rows;
+    const int dim0 = lane * EPL;
+    float x[EPL];
+    float amax = 0.f;
+    if (row < p.n) {
+        __nv_bfloat16 qb[EPL];
+        const size_t src = (static_cast<size_t>(row) * p.H + h) * D + dim0;
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint2*>(qb) = *reinterpret_cast<const uint2*>(p.q + src);
+        else
+            *reinterpret_cast<uint32_t*>(qb) = *reinterpret_cast<const uint32_t*>(p.q + src);
+#pragma unroll
+        for (int j = 0; j < EPL / 2; ++j) {
+            const float2 cs = p.rope[static_cast<size_t>(row) * (D / 2) + dim0 / 2 + j];
+            rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), cs.x, cs.y, x[2 * j],
+                        x[2 * j + 1]);
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x[e] = 0.f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sq = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
+    const float inv = __frcp_rn(sq);
+    float r[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) r[e] = x[e] * inv;
+    const int mt = row / kMTile, rr = row - mt * kMTile;
+#pragma unroll
+    for (int pc = 0; pc < kQPieces; ++pc) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) {
+            const uint32_t two = e4m3x2(r[e], r[e + 1]);
+            const float2 back = e4m3x2_to_float2(static_cast<uint16_t>(two));
+            r[e] -= back.x;
+            r[e + 1] -= back.y;
+            word |= two << (8 * e);
+        }
+        uint8_t* dst = p.qp + ((static_cast<size_t>(h) * p.nmt + mt) * kQPieces + pc) * (kMTile * D);
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint32_t*>(dst + ktile_off(rr, dim0, D)) = word;
+        else
+            *reinterpret_cast<uint16_t*>(dst + ktile_off(rr, dim0, D)) = static_cast<uint16_t>(word);
+    }
+    if (lane == 0) p.qs[static_cast<size_t>(h) * rows + row] = sq;
+}
+
+template <int D>
+static cudaError_t launch_q_prep_d(const QPrepParams& p, cudaStream_t s) {
+    const int rows = p.nmt * kMTile;
+    const int nrb = (p.H * rows + kPrepWarps - 1) / kPrepWarps;
+    q_prep_kernel<D><<<nrb + p.H, kPrepWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q_prep(const QPrepParams& p, int D, cudaStream_t s) {
+    return (D == 128) ? launch_q_prep_d<128>(p, s) : launch_q_prep_d<64>(p, s);
+}
+
+// ---------------------------------------------------------------- K4 attention
+
 // Every lane waits; the warp continues only if all lanes saw the phase.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState ab, int where) {
     const bool ok = mbar_wait(bar, parity, ab, where);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Four E4M3 codes (one 32-bit word) -> four fp16 holding code / 256, exactly:
+// E4M3 s.eeee.mmm and fp16 s.eeeee.mmmmmmmmmm share the layout once the
+// magnitude bits sit at fp16 bits 7..13, and the exponent bias differs by 8.
+__device__ __forceinline__ void e4m3x4_to_f16x4_div256(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t a = __byte_perm(w, 0u, 0x1404);  // codes 0, 1 in bytes 1 and 3
+    const uint32_t b = __byte_perm(w, 0u, 0x3424);  // codes 2, 3 in bytes 1 and 3
+    lo = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
+    hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
 }
 
 template <int D>
@@ -77,7 +193,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);  // [0] tmem, [1] svmax, [2] abort
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);  // [0] tmem, [2] abort
+    const float* s_sq = reinterpret_cast<const float*>(smem + Lay::kSq);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y;
@@ -99,7 +216,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             mbar_init(&bars[B_O_DONE + i], 1);
         }
         mbar_init(&bars[B_DRAIN], 1);
-        misc[1] = 0u;
+        mbar_init(&bars[B_Q_FULL], 1);
         misc[2] = 0u;
         fence_mbar_init();
     }
@@ -107,97 +224,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         tmem_alloc(&misc[0], kTmemCols);
         tmem_relinquish();
     }
-
-    // softmax groups: rotate their Q rows, split into three E4M3 pieces
-    const bool is_sm = (warp >= kWarpSm0) && (warp < kWarpSm0 + 8);
-    const int mt = is_sm ? (warp - kWarpSm0) >> 2 : 0;    // M tile of this softmax group
-    const int quad = warp & 3;                             // TMEM lane quadrant
-    const int r = quad * 32 + lane;                        // row within the M tile
-    const int grow = row0 + mt * kMTile + r;               // query row
-    float qscale = 1.f;
-    if (is_sm) {
-        uint8_t* qdst[kQPieces];
-#pragma unroll
-        for (int pc = 0; pc < kQPieces; ++pc) qdst[pc] = smem + Lay::kQ + (pc * 2 + mt) * (kMTile * D);
-        if (grow < p.n) {
-            const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(grow) * p.H + h) * D;
-            const float2* rrow = p.rope + static_cast<size_t>(grow) * (D / 2);
-            float amax = 0.f;
-            for (int c = 0; c < D / 16; ++c) {
-                uint4 qa = *reinterpret_cast<const uint4*>(qrow + c * 16);
-                uint4 qb = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
-                const __nv_bfloat16* qv0 = reinterpret_cast<const __nv_bfloat16*>(&qa);
-                const __nv_bfloat16* qv1 = reinterpret_cast<const __nv_bfloat16*>(&qb);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float2 cs = rrow[c * 8 + j];
-                    const __nv_bfloat16* src = (j < 4) ? qv0 : qv1;
-                    float x, y;
-                    rotate_pair(__bfloat162float(src[(2 * j) & 7]), __bfloat162float(src[(2 * j + 1) & 7]), cs.x,
-                                cs.y, x, y);
-                    amax = fmaxf(amax, fmaxf(fabsf(x), fabsf(y)));
-                }
-            }
-            qscale = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
-            const float inv = __frcp_rn(qscale);
-            for (int c = 0; c < D / 16; ++c) {
-                uint4 qa = *reinterpret_cast<const uint4*>(qrow + c * 16);
-                uint4 qb = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
-                const __nv_bfloat16* qv0 = reinterpret_cast<const __nv_bfloat16*>(&qa);
-                const __nv_bfloat16* qv1 = reinterpret_cast<const __nv_bfloat16*>(&qb);
-                uint32_t w[kQPieces][4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float2 cs = rrow[c * 8 + j];
-                    const __nv_bfloat16* src = (j < 4) ? qv0 : qv1;
-                    float x, y;
-                    rotate_pair(__bfloat162float(src[(2 * j) & 7]), __bfloat162float(src[(2 * j + 1) & 7]), cs.x,
-                                cs.y, x, y);
-                    float rx = x * inv, ry = y * inv;
-#pragma unroll
-                    for (int pc = 0; pc < kQPieces; ++pc) {
-                        const uint32_t two = e4m3x2(rx, ry);
-                        const float2 back = e4m3x2_to_float2(static_cast<uint16_t>(two));
-                        rx -= back.x;
-                        ry -= back.y;
-                        if ((j & 1) == 0)
-                            w[pc][j >> 1] = two;
-                        else
-                            w[pc][j >> 1] |= two << 16;
-                    }
-                }
-#pragma unroll
-                for (int pc = 0; pc < kQPieces; ++pc)
-                    *reinterpret_cast<uint4*>(qdst[pc] + ktile_off(r, c * 16, D)) =
-                        make_uint4(w[pc][0], w[pc][1], w[pc][2], w[pc][3]);
-            }
-        } else {
-            for (int c = 0; c < D / 16; ++c)
-#pragma unroll
-                for (int pc = 0; pc < kQPieces; ++pc)
-                    *reinterpret_cast<uint4*>(qdst[pc] + ktile_off(r, c * 16, D)) = make_uint4(0, 0, 0, 0);
-        }
-        fence_async_smem();  // the MMA reads these rows through the async proxy
-    }
-    // converter group: the head's largest V scale (the P.V operand reference)
-    if (warp >= kWarpCvt) {
-        float m = 0.f;
-        for (int i = tid - kWarpCvt * 32; i < p.C; i += 128) m = fmaxf(m, p.sv[static_cast<size_t>(h) * p.Cpad + i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) atomicMax(&misc[1], __float_as_uint(m));
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const float svmax = __uint_as_float(misc[1]);
 
     auto stage_ptr = [&](int s) { return smem + Lay::kStage0 + s * Lay::kStageBytes; };
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
+            // the prepared query pieces, row scales and the head's largest V scale
+            uint64_t* qf = &bars[B_Q_FULL];
+            mbar_arrive_expect_tx(qf, kQPieces * 2 * kMTile * D + 2 * kMTile * 4 + 16);
+            const int mt0 = blockIdx.x * 2;
+            for (int pc = 0; pc < kQPieces; ++pc)
+                for (int i = 0; i < 2; ++i)
+                    bulk_g2s(smem + Lay::kQ + (pc * 2 + i) * (kMTile * D),
+                             p.qp + ((static_cast<size_t>(h) * p.nmt + mt0 + i) * kQPieces + pc) * (kMTile * D),
+                             kMTile * D, qf);
+            bulk_g2s(smem + Lay::kSq, p.qs + static_cast<size_t>(h) * p.nmt * kMTile + mt0 * kMTile, 2 * kMTile * 4,
+                     qf);
+            bulk_g2s(smem + Lay::kSq + 2 * kMTile * 4, p.svm + h * 4, 16, qf);
             const uint32_t bytes = 2 * Lay::kTile + 1024 + (p.masked ? 512 : 0);
             for (int j = 0; j < T; ++j) {
                 const int s = j & 1;
@@ -213,15 +261,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 if (p.masked) bulk_g2s(st + 2 * Lay::kTile + 1024, p.grp + j * kTileSlots, 512, full);
             }
             if (*ab.flag) {
-                // leave no copy in flight: wait (bounded) for the last fill of each stage
-                AbortState quiet{ab.flag, ab.status};
+                // leave no copy in flight: wait (bounded) for the query copies and
+                // the last fill of each stage
+                uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&bars[B_Q_FULL], 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
                 for (int s = 0; s < kStages && s < T; ++s) {
                     const int last = ((T - 1 - s) / kStages) * kStages + s;
-                    uint64_t t0 = global_timer_ns();
+                    t0 = global_timer_ns();
                     while (!mbar_try_wait(&bars[B_KV_FULL + s], (last >> 1) & 1) &&
                            global_timer_ns() - t0 < 100000000ull) {
                     }
-                    (void)quiet;
                 }
             }
         }
@@ -253,7 +303,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     mma_f16_ts(d_tmem, a_tmem + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = true;
+            bool ok = mbar_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutMma);
             for (int j = 0; j < T && ok; ++j) {
                 const int s = j & 1;
                 ok = mbar_wait(&bars[B_KV_FULL + s], (j >> 1) & 1, ab, kDevTimeoutMma);
@@ -287,16 +337,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             while (!mbar_try_wait(&bars[B_DRAIN], 0) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
-    } else if (is_sm) {
+    } else if (warp < kWarpCvt) {
         // ------------------------------------------------------------ softmax
+        // Row r of M tile mt; scores in log2 units: x = S * sk_col * a with
+        // a = sq_row * log2(e)/sqrt(D).  P'' = exp2(x - m - log2(max sv)), so
+        // P' = P'' * sv_col = p * sv_col / max sv stays <= 2^8 in fp16 and the
+        // shift cancels in out = O / sum(P'').  The running max m only moves
+        // (with an O rescale) when a tile raises it by more than 8.
+        const int mt = (warp - kWarpSm0) >> 2;    // M tile of this softmax group
+        const int quad = warp & 3;                 // TMEM lane quadrant
+        const int r = quad * 32 + lane;            // row within the M tile
+        const int grow = row0 + mt * kMTile + r;   // query row
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + 128u * mt;
         const uint32_t o_tm = tmem + lane_off + 256u + static_cast<uint32_t>(D) * mt;
-        const float a = qscale * p.sm_log2;  // > 0
-        const float inv_svmax = (svmax > 0.f) ? __frcp_rn(svmax) : 1.f;
+        bool ok = warp_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutSoftmax);
+        const float a = ok ? s_sq[mt * kMTile + r] * p.sm_log2 : 0.f;  // > 0
+        const float svmax = ok ? s_sq[2 * kMTile] : 1.f;
+        const float lsv = (svmax > 0.f) ? lg2_approx(svmax) : 0.f;
+        const float2 a2 = make_float2(a, a);
         float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < T; ++j) {
+        for (int j = 0; j < T && ok; ++j) {
             const int s = j & 1;
             ok = warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax);
             if (ok) ok = warp_wait(&bars[B_KV_FULL + s], (j >> 1) & 1, ab, kDevTimeoutSoftmax);
@@ -308,40 +369,109 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             const int32_t* sgrp = reinterpret_cast<const int32_t*>(ssv + kTileSlots);
             const int nvalid = min(kTileSlots, p.C - j * kTileSlots);
             const bool full = (nvalid == kTileSlots) && !p.masked;
-            auto valid = [&](int col) { return full || (col < nvalid && (!p.masked || sgrp[col] >= 0)); };
-            // pass A: the tile's largest scaled score
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_tm + 32 * c, v);
+            auto valid = [&](int col) { return col < nvalid && (!p.masked || sgrp[col] >= 0); };
+
+            // pass A: the tile's largest score (in units of a).  32-column TMEM
+            // loads are double-buffered: the next chunk loads while this one is used.
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            auto max_chunk = [&](const uint32_t (&v)[32], int c) {
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int col = 32 * c + k;
-                    const float x = valid(col) ? __uint_as_float(v[k]) * ssk[col] : -INFINITY;
-                    mx = fmaxf(mx, x);
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
+                        const float2 x0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                               make_float2(s4.x, s4.y));
+                        const float2 x1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                               make_float2(s4.z, s4.w));
+                        mx[(k >> 2) & 1] = max3(mx[(k >> 2) & 1], x0.x, x0.y);
+                        mx[2 + ((k >> 2) & 1)] = max3(mx[2 + ((k >> 2) & 1)], x1.x, x1.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = 32 * c + k;
+                        if (valid(col)) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]) * ssk[col]);
+                    }
                 }
+            };
+            {
+                uint32_t va[32], vb[32];
+                tmem_ld32_async(s_tm, va);
+                tmem_wait_ld_dep(va);
+                tmem_ld32_async(s_tm + 32, vb);
+                max_chunk(va, 0);
+                tmem_wait_ld_dep(vb);
+                tmem_ld32_async(s_tm + 64, va);
+                max_chunk(vb, 1);
+                tmem_wait_ld_dep(va);
+                tmem_ld32_async(s_tm + 96, vb);
+                max_chunk(va, 2);
+                tmem_wait_ld_dep(vb);
+                max_chunk(vb, 3);
             }
-            const float m_new = fmaxf(m_run, mx * a);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_run - m_use);
-            // pass B: probabilities, row sum, fp16 P (with the V scale) over S
-            float l_tile = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_tm + 32 * c, v);
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
+            const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+            const float m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+            const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = bump ? ex2(m_run - m_fin) : 1.f;
+            const float msub = m_fin + lsv;
+            const float2 nm2 = make_float2(-msub, -msub);
+
+            // pass B: probabilities, row sum, fp16 P' written over the chunk's S
+            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            auto p_chunk = [&](const uint32_t (&v)[32], int c) {
                 uint32_t pk[16];
+                if (full) {
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2) {
-                    const int c0 = 32 * c + 2 * k2, c1 = c0 + 1;
-                    const float p0 = valid(c0) ? ex2(__fmaf_rn(__uint_as_float(v[2 * k2]) * ssk[c0], a, -m_use)) : 0.f;
-                    const float p1 = valid(c1) ? ex2(__fmaf_rn(__uint_as_float(v[2 * k2 + 1]) * ssk[c1], a, -m_use)) : 0.f;
-                    l_tile += p0 + p1;
-                    __half2 hp = __floats2half2_rn(p0 * (ssv[c0] * inv_svmax), p1 * (ssv[c1] * inv_svmax));
-                    pk[k2] = *reinterpret_cast<uint32_t*>(&hp);
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
+                        const float4 v4 = *reinterpret_cast<const float4*>(ssv + 32 * c + k);
+                        const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                                    make_float2(s4.x, s4.y)), a2, nm2);
+                        const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                                    make_float2(s4.z, s4.w)), a2, nm2);
+                        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                        ls[0] = add2(ls[0], p0);
+                        ls[1] = add2(ls[1], p1);
+                        const float2 q0 = mul2(p0, make_float2(v4.x, v4.y));
+                        const float2 q1 = mul2(p1, make_float2(v4.z, v4.w));
+                        __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+                        __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
+                        pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const int c0 = 32 * c + k, c1 = c0 + 1;
+                        const float p0 = valid(c0) ? ex2(__fmaf_rn(__uint_as_float(v[k]) * ssk[c0], a, -msub)) : 0.f;
+                        const float p1 =
+                            valid(c1) ? ex2(__fmaf_rn(__uint_as_float(v[k + 1]) * ssk[c1], a, -msub)) : 0.f;
+                        ls[0].x += p0;
+                        ls[1].y += p1;
+                        __half2 hp = __floats2half2_rn(p0 * ssv[c0], p1 * ssv[c1]);
+                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
+                    }
                 }
+                // P chunk c (32 slots as 16 fp16 pairs) goes to columns 16c..16c+15,
+                // which were read in chunks <= c
                 tmem_st16(s_tm + 16 * c, pk);
+            };
+            {
+                uint32_t va[32], vb[32];
+                tmem_ld32_async(s_tm, va);
+                tmem_wait_ld_dep(va);
+                tmem_ld32_async(s_tm + 32, vb);
+                p_chunk(va, 0);
+                tmem_wait_ld_dep(vb);
+                tmem_ld32_async(s_tm + 64, va);
+                p_chunk(vb, 1);
+                tmem_wait_ld_dep(va);
+                tmem_ld32_async(s_tm + 96, vb);
+                p_chunk(va, 2);
+                tmem_wait_ld_dep(vb);
+                p_chunk(vb, 3);
             }
             tmem_st_wait();
             __syncwarp();
@@ -358,7 +488,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 }
                 tmem_st_wait();
             }
-            l_run = l_run * alpha + l_tile;
+            l_run = l_run * alpha + ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y));
             m_run = m_new;
             tc_fence_before();
             __syncwarp();
@@ -368,7 +498,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         if (ok) ok = warp_wait(&bars[B_O_DONE + mt], 0, ab, kDevTimeoutEpilogue);
         if (ok) {
             tc_fence_after();
-            const float fin = (l_run > 0.f) ? svmax / l_run : 0.f;
+            const float fin = (l_run > 0.f) ? kV16Scale / l_run : 0.f;
             float* orow = p.out + (static_cast<size_t>(grow) * p.H + h) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -383,7 +513,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 }
             }
         }
-    } else if (warp >= kWarpCvt) {
+    } else {
         // ------------------------------------------------------------ V converter
         const int ct = tid - kWarpCvt * 32;
         uint8_t* v16 = smem + Lay::kV16;
@@ -393,20 +523,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             if (ok) ok = warp_wait(&bars[B_V16_EMPTY], (j & 1) ^ 1, ab, kDevTimeoutConvert);
             if (!ok) break;
             const uint8_t* v8 = stage_ptr(s) + Lay::kTile;
-#pragma unroll 2
+#pragma unroll 4
             for (int u = ct; u < D * 8; u += 128) {
                 const int rr = u >> 3, cp = u & 7;
                 const uint4 raw = *reinterpret_cast<const uint4*>(v8 + rr * 128 + cp * 16);
                 const int c = cp ^ (rr & 7);  // logical 16-slot chunk
-                const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
                 uint32_t o[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    __half2_raw lo = e4m3x2_to_half2(static_cast<uint16_t>(in[q] & 0xFFFFu));
-                    __half2_raw hi = e4m3x2_to_half2(static_cast<uint16_t>(in[q] >> 16));
-                    o[2 * q] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-                    o[2 * q + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-                }
+                e4m3x4_to_f16x4_div256(raw.x, o[0], o[1]);
+                e4m3x4_to_f16x4_div256(raw.y, o[2], o[3]);
+                e4m3x4_to_f16x4_div256(raw.z, o[4], o[5]);
+                e4m3x4_to_f16x4_div256(raw.w, o[6], o[7]);
                 uint8_t* dst = v16 + (c >> 2) * (D * 128) + rr * 128;
                 const int l0 = 2 * (c & 3);
                 *reinterpret_cast<uint4*>(dst + (((l0) ^ (rr & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -441,7 +567,7 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid((p.n + kRowsPerCta - 1) / kRowsPerCta, p.H);
+    dim3 grid(p.nmt / 2, p.H);
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

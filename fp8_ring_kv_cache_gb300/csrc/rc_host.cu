@@ -59,6 +59,10 @@ struct rc_cache {
     uint8_t* d_rt_vt = nullptr;
     float* d_rt_sk = nullptr;
     float* d_rt_sv = nullptr;
+    uint8_t* d_qp = nullptr;   // prepared query pieces of one attention call
+    float* d_qs = nullptr;     // their row scales
+    float* d_svm = nullptr;    // per-head largest V scale
+    int nmt_max = 0;           // 128-row query tiles for max_write queries (even)
     RopeEntry pool[kPoolEntries];
     uint64_t clock = 0;
     // host mirrors of the ring tables
@@ -104,6 +108,9 @@ void free_all(rc_cache* h) {
     cudaFree(h->d_rt_vt);
     cudaFree(h->d_rt_sk);
     cudaFree(h->d_rt_sv);
+    cudaFree(h->d_qp);
+    cudaFree(h->d_qs);
+    cudaFree(h->d_svm);
     for (auto& e : h->pool) {
         cudaFree(e.d_table);
         cudaFree(e.d_pos);
@@ -112,6 +119,8 @@ void free_all(rc_cache* h) {
     }
     delete h;
 }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool is_arith(const int64_t* p, int n) {
     for (int t = 1; t < n; ++t)
@@ -248,6 +257,10 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     st |= dmalloc(&h->d_grp, static_cast<size_t>(h->L) * h->Cpad);
     st |= dmalloc(&h->d_theta, static_cast<size_t>(h->D / 2));
     st |= dmalloc(&h->d_status, 1);
+    h->nmt_max = 2 * ((h->max_write + 255) / 256);
+    st |= dmalloc(&h->d_qp, static_cast<size_t>(h->H) * h->nmt_max * 3 * 128 * h->D);
+    st |= dmalloc(&h->d_qs, static_cast<size_t>(h->H) * h->nmt_max * 128);
+    st |= dmalloc(&h->d_svm, static_cast<size_t>(h->H) * 4);
     for (auto& e : h->pool) {
         st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
         st |= dmalloc(&e.d_pos, static_cast<size_t>(h->max_write));
@@ -320,6 +333,7 @@ void rc_cache_destroy(rc_cache* h) {
 int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf16, const int64_t* positions, int n,
                    void* stream) {
     if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
+    if (!aligned16(K_bf16) || !aligned16(V_bf16)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // distinct slots
@@ -376,6 +390,8 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     wp.pos = re.arith ? nullptr : re.d_pos;
     wp.p0 = positions[0];
     wp.delta_total = h->delta_total;
+    wp.slot0 = static_cast<int>(floormod(positions[0] - h->delta_total, h->C));
+    wp.status = h->d_status;
     wp.n = n;
     wp.H = h->H;
     wp.C = h->C;
@@ -432,6 +448,7 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
 static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out, int n, void* stream,
                          bool readtime) {
     if (!h || !Q_bf16 || !out) return RC_ERR_ARG;
+    if (!aligned16(Q_bf16) || !aligned16(out)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1) return RC_ERR_ARG;
     if (h->last_n[layer] == 0 || n != h->last_n[layer] || h->occupancy[layer] == 0) return RC_ERR_STATE;
     if (readtime && !h->ablation) return RC_ERR_STATE;
@@ -480,6 +497,26 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
         ap.sv = h->d_sv + lsc;
     }
     ap.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
+    // query preparation: rotated, scaled, split into E4M3 pieces in the
+    // attention kernel's shared-memory layout; and each head's largest V scale
+    QPrepParams qp{};
+    qp.q = static_cast<const __nv_bfloat16*>(Q_bf16);
+    qp.rope = h->pool[entry].d_table;
+    qp.sv = ap.sv;
+    qp.qp = h->d_qp;
+    qp.qs = h->d_qs;
+    qp.svm = h->d_svm;
+    qp.n = n;
+    qp.H = h->H;
+    qp.C = h->C;
+    qp.Cpad = h->Cpad;
+    qp.nmt = 2 * ((n + 255) / 256);
+    if (launch_q_prep(qp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    ap.qp = h->d_qp;
+    ap.qs = h->d_qs;
+    ap.svm = h->d_svm;
+    ap.nmt = qp.nmt;
     ap.q = static_cast<const __nv_bfloat16*>(Q_bf16);
     ap.rope = h->pool[entry].d_table;
     ap.out = out;

@@ -30,14 +30,16 @@ struct WriteParams {
     const __nv_bfloat16* K;  // [n][H][D]
     const __nv_bfloat16* V;
     const float2* rope;    // [n][D/2]
-    const int64_t* pos;    // device positions or nullptr
+    const int64_t* pos;    // device positions or nullptr (arithmetic run)
     int64_t p0;
     int64_t delta_total;
+    int slot0;             // floormod(p0 - delta_total, C) when pos is nullptr
     int n, H, C, T, Cpad;
     int32_t group;         // compact write-group index of this write
     __nv_bfloat16* kraw;   // read-time store [H][Cpad][D] (nullptr if off)
     __nv_bfloat16* vraw;
     float2* slot_rope;     // read-time store [Cpad][D/2] (nullptr if off)
+    int* status;           // device status word (bounded waits)
 };
 
 // K3: in-place delta rotation with per-(layer, head, group) requantisation.
@@ -63,6 +65,20 @@ struct ReadtimeParams {
     int H, C, T, Cpad;
 };
 
+// K6: query preparation for one attention call: RoPE at the query positions,
+// one fp32 scale per (token, head) row, three E4M3 pieces per element laid out
+// as the swizzled shared-memory image of the attention kernel's A operand;
+// and the largest V scale of every head.
+struct QPrepParams {
+    const __nv_bfloat16* q;  // [n][H][D]
+    const float2* rope;      // [n][D/2]
+    const float* sv;         // layer [H][Cpad]
+    uint8_t* qp;             // [H][nmt][3][128][D] (rows >= n are zero)
+    float* qs;               // [H][nmt * 128] row scales (1 for rows >= n)
+    float* svm;              // [H][4] largest V scale (element 0)
+    int n, H, C, Cpad, nmt;  // nmt: 128-row M tiles, rounded up to even
+};
+
 // K4: FP8 attention over one layer's ring.
 struct AttnParams {
     const uint8_t* kc;     // layer [H][T][128][D]
@@ -73,6 +89,10 @@ struct AttnParams {
     const __nv_bfloat16* q;  // [n][H][D]
     const float2* rope;    // [n][D/2]
     float* out;            // [n][H][D]
+    const uint8_t* qp;     // prepared query pieces (QPrepParams::qp)
+    const float* qs;       // row scales
+    const float* svm;      // per-head largest V scale
+    int nmt;               // M tiles in qp / qs (even)
     int n, H, C, T, Cpad;
     int masked;            // 1: some slots are empty, read grp
     float sm_log2;         // log2(e) / sqrt(D)
@@ -83,6 +103,7 @@ cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t s);
 cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s);
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status);
 cudaError_t launch_readtime(const ReadtimeParams& p, int D, cudaStream_t s);
+cudaError_t launch_q_prep(const QPrepParams& p, int D, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, cudaStream_t s);
 
 // Status values a kernel writes into the device status word.

@@ -58,6 +58,7 @@ extern "C" int rc_ring_write_noalloc(const rc_ring_view* ring, const void* K_bf1
                                      const int64_t* positions, int n, int64_t delta_total, int32_t group,
                                      double rope_base, void* stream) {
     if (!ring || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(K_bf16) & 15u) || (reinterpret_cast<uintptr_t>(V_bf16) & 15u)) return RC_ERR_ARG;
     if (!ring->kcodes || !ring->vcodes || !ring->kscale || !ring->vscale || !ring->group) return RC_ERR_ARG;
     if (ring->heads < 1 || ring->slots < 1 || !(rope_base > 1.0) || group < 0) return RC_ERR_ARG;
     if (ring->head_dim != 64 && ring->head_dim != 128) return RC_ERR_UNSUPPORTED;
@@ -112,6 +113,8 @@ extern "C" int rc_ring_write_noalloc(const rc_ring_view* ring, const void* K_bf1
     wp.pos = arith ? nullptr : dpos;
     wp.p0 = positions[0];
     wp.delta_total = delta_total;
+    wp.slot0 = static_cast<int>(floormod(positions[0] - delta_total, C));
+    wp.status = nullptr;
     wp.n = n;
     wp.H = ring->heads;
     wp.C = C;

@@ -2,13 +2,14 @@
 //
 // K3 rotate_kernel (paperdot abstract: "a delta rotation when positions
 //    reset"): every stored key moves from position p to p + delta in place.
-//    One cluster of 8 CTAs per (layer, head); each CTA bulk-copies its run of
-//    tiles (codes, slot scales, slot groups) into shared memory, dequantises and
-//    rotates each row by delta, and reduces the amax of every write group in a
-//    shared-memory table; the cluster merges the tables through distributed
-//    shared memory; then each row is requantised with its group's new scale
-//    s = fl32(amax / 448) and written back.  One read and one write of the K
-//    codes; V is not touched.
+//    One cluster of 8 CTAs per (layer, head); each thread owns one 16-byte
+//    chunk (16 codes) of its rows, dequantises and rotates it by delta, and
+//    keeps a running amax per write group that it flushes into a shared-memory
+//    table when the group changes; the cluster merges the tables through
+//    distributed shared memory; then every row is requantised with its group's
+//    new scale s = fl32(amax / 448) and written back.  The second pass re-reads
+//    the codes the CTA has just read (an L2 hit), so HBM sees one read and one
+//    write of the K codes; V is not touched.
 // K5 readtime_kernel (the original read-time design the abstract and the
 //    cpdf.ai section "Como rodar 57B em tempo real com batch size 1" describe):
 //    rebuilds one layer's FP8 ring from the unrotated bf16 store -- RoPE at each
@@ -20,7 +21,7 @@
 namespace rc {
 
 constexpr int kRotCluster = 8;
-constexpr int kRotWarps = 16;
+constexpr int kRotWarps = 8;
 constexpr int kRotThreads = kRotWarps * 32;
 
 // EPL consecutive codes of one row -> fp32 (exact), EPL = 4 or 2.
@@ -65,142 +66,159 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// shared-memory carve-up of the rotate kernel
-struct RotSmem {
-    uint32_t codes, sk, grp, gmax, bar, total;
-};
-__host__ __device__ inline RotSmem rot_smem(int tpc, int D, int Cpad) {
-    RotSmem s;
-    s.codes = 0;
-    s.sk = s.codes + tpc * kTileSlots * D;
-    s.grp = s.sk + tpc * kTileSlots * 4;
-    s.gmax = s.grp + tpc * kTileSlots * 4;
-    s.bar = s.gmax + ((Cpad * 4 + 15) / 16) * 16;
-    s.total = s.bar + 16;
-    return s;
+// 16 E4M3 codes (one 16-byte chunk) -> 8 (x, y) pairs in fp32, exact.
+__device__ __forceinline__ void decode16(const uint4 raw, float2 (&v)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = e4m3x2_to_float2(static_cast<uint16_t>(w[q] & 0xFFFFu));
+        v[2 * q + 1] = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> 16));
+    }
+}
+
+// (a, b) -> (a c - b s, a s + b c) in the same rounding order as rotate_pair:
+// the (-b s, b c) products are rounded first, then fused into a (c, s).
+__device__ __forceinline__ float2 rotate2(float2 ab, float2 cs, float2 sc) {
+    return fma2(make_float2(ab.x, ab.x), cs, mul2(make_float2(-ab.y, ab.y), sc));
 }
 
 template <int D>
-__global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThreads, 1)
+__global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThreads)
     rotate_kernel(RotateParams p, int tpc, int* status) {
-    constexpr int EPL = D / 32;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint32_t abort_flag;
-    const RotSmem L = rot_smem(tpc, D, p.Cpad);
-    uint8_t* sc = smem + L.codes;
-    float* ssk = reinterpret_cast<float*>(smem + L.sk);
-    int32_t* sgrp = reinterpret_cast<int32_t*>(smem + L.grp);
-    uint32_t* gmax = reinterpret_cast<uint32_t*>(smem + L.gmax);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    constexpr int CPR = D / 16;                 // 16-byte chunks per row
+    constexpr int RPI = kRotThreads / CPR;      // rows per pass of the CTA
+    extern __shared__ __align__(16) uint32_t gmax[];  // [Cpad] group amax (fp32 bits)
+    (void)status;
 
     const int crank = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int dim0 = lane * EPL;
+    const int tid = threadIdx.x;
+    const int chunk = tid % CPR;                // logical chunk: dims 16*chunk .. +15
+    const int rsub = tid / CPR;
     const int tile0 = min(p.T, crank * tpc);
     const int ntiles = min(p.T, tile0 + tpc) - tile0;
-    const int nrows = max(0, min(p.C - tile0 * kTileSlots, ntiles * kTileSlots));
+    const int row0 = tile0 * kTileSlots;
+    const int nrows = max(0, min(p.C - row0, ntiles * kTileSlots));
     const size_t lh = static_cast<size_t>(l) * p.H + h;
     uint8_t* gkc = p.kc + (lh * p.T + tile0) * static_cast<size_t>(kTileSlots * D);
-    float* gsk = p.sk + lh * p.Cpad + static_cast<size_t>(tile0) * kTileSlots;
-    const int32_t* ggrp = p.grp + static_cast<size_t>(l) * p.Cpad + static_cast<size_t>(tile0) * kTileSlots;
+    float* gsk = p.sk + lh * p.Cpad + row0;
+    const int32_t* ggrp = p.grp + static_cast<size_t>(l) * p.Cpad + row0;
 
-    if (tid == 0) {
-        abort_flag = 0;
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    for (int i = tid; i < p.Cpad; i += kRotThreads) gmax[i] = 0u;
+    // (cos, sin) and (sin, cos) of this thread's 8 pairs, read through shared
+    // memory: indexing the parameter array per thread would serialise on the
+    // constant cache every time the compiler reloads it
+    __shared__ float2 s_cs[kMaxHalfDim];
+    if (tid < D / 2) s_cs[tid] = p.cs[tid];
     __syncthreads();
-    if (tid == 0 && ntiles > 0) {
-        const uint32_t nb = static_cast<uint32_t>(ntiles) * kTileSlots;
-        mbar_arrive_expect_tx(bar, nb * D + nb * 8);
-        bulk_g2s(sc, gkc, nb * D, bar);
-        bulk_g2s(ssk, gsk, nb * 4, bar);
-        bulk_g2s(sgrp, ggrp, nb * 4, bar);
+    float2 cs[8], sc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        cs[j] = s_cs[chunk * 8 + j];
+        sc[j] = make_float2(cs[j].y, cs[j].x);
     }
+    auto chunk_addr = [&](int r) {
+        return gkc + (r >> 7) * (kTileSlots * D) + ktile_off(r & 127, chunk * 16, D);
+    };
+
+    for (int i = tid; i < p.Cpad; i += kRotThreads) gmax[i] = 0u;
     cluster_sync();  // every CTA's table is zero before anyone merges into rank 0
-    AbortState ab{&abort_flag, status};
-    bool ok = true;
-    if (ntiles > 0) ok = mbar_wait(bar, 0, ab, kDevTimeoutLoader);
 
-    float cs_c[EPL / 2], cs_s[EPL / 2];
+    // ---- phase 1: rotated amax per write group (running max, flushed per group run);
+    // four rows per thread are loaded before any is used, to keep loads in flight
+    constexpr int kBatch = 4;
+    float acc = 0.f, scur = 0.f;
+    int gcur = -1;
+    for (int rb = rsub; rb < nrows; rb += kBatch * RPI) {
+        uint4 raw[kBatch];
+        int grow[kBatch];
 #pragma unroll
-    for (int j = 0; j < EPL / 2; ++j) {
-        cs_c[j] = p.cs[dim0 / 2 + j].x;
-        cs_s[j] = p.cs[dim0 / 2 + j].y;
-    }
-
-    // ---- phase 1: rotated amax per write group (code space times the slot scale)
-    if (ok) {
-        for (int r = warp; r < nrows; r += kRotWarps) {
-            const int g = sgrp[r];
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = rb + b * RPI;
+            grow[b] = (r < nrows) ? ggrp[r] : -1;
+            if (grow[b] >= 0) raw[b] = *reinterpret_cast<const uint4*>(chunk_addr(r));
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int g = grow[b];
             if (g < 0) continue;
-            float y[EPL];
-            decode_codes<EPL>(load_codes<EPL>(sc + (r >> 7) * (kTileSlots * D) + ktile_off(r & 127, dim0, D)), y);
-            float am = 0.f;
-#pragma unroll
-            for (int j = 0; j < EPL / 2; ++j) {
-                float a, b;
-                rotate_pair(y[2 * j], y[2 * j + 1], cs_c[j], cs_s[j], a, b);
-                am = fmaxf(am, fmaxf(fabsf(a), fabsf(b)));
+            if (g != gcur) {
+                if (gcur >= 0) atomicMax(&gmax[gcur], __float_as_uint(acc * scur));
+                gcur = g;
+                scur = gsk[rb + b * RPI];
+                acc = 0.f;
             }
-            am = warp_max(am);
-            if (lane == 0) atomicMax(&gmax[g], __float_as_uint(am * ssk[r]));
+            float2 v[8];
+            decode16(raw[b], v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 x = rotate2(v[j], cs[j], sc[j]);
+                acc = max3(acc, fabsf(x.x), fabsf(x.y));
+            }
         }
     }
+    if (gcur >= 0) atomicMax(&gmax[gcur], __float_as_uint(acc * scur));
     __syncthreads();
     // ---- merge the tables into cluster rank 0 (one push per run of equal groups)
     if (crank != 0) {
         for (int r = tid; r < nrows; r += kRotThreads) {
-            const int g = sgrp[r];
-            if (g >= 0 && (r == 0 || sgrp[r - 1] != g)) dsmem_max_u32(map_shared(&gmax[g], 0), gmax[g]);
+            const int g = ggrp[r];
+            if (g >= 0 && (r == 0 || ggrp[r - 1] != g)) dsmem_max_u32(map_shared(&gmax[g], 0), gmax[g]);
         }
     }
     cluster_sync();
     if (crank != 0) {
         for (int r = tid; r < nrows; r += kRotThreads) {
-            const int g = sgrp[r];
-            if (g >= 0 && (r == 0 || sgrp[r - 1] != g)) gmax[g] = dsmem_ld_u32(map_shared(&gmax[g], 0));
+            const int g = ggrp[r];
+            if (g >= 0 && (r == 0 || ggrp[r - 1] != g)) gmax[g] = dsmem_ld_u32(map_shared(&gmax[g], 0));
         }
     }
     cluster_sync();  // rank 0's table is not read after this point
-    // ---- phase 2: requantise with the group's new scale and write back
-    if (ok) {
-        for (int r = warp; r < nrows; r += kRotWarps) {
-            const int g = sgrp[r];
+    // ---- phase 2: requantise with the group's new scale and write back (codes re-read from L2)
+    for (int rb = rsub; rb < nrows; rb += kBatch * RPI) {
+        uint4 raw[kBatch];
+        int grow[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = rb + b * RPI;
+            grow[b] = (r < nrows) ? ggrp[r] : -1;
+            if (grow[b] >= 0) raw[b] = *reinterpret_cast<const uint4*>(chunk_addr(r));
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int g = grow[b];
             if (g < 0) continue;
+            const int r = rb + b * RPI;
             const float amax = __uint_as_float(gmax[g]);
             const float s_new = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
-            const float mult = __fdiv_rn(ssk[r], s_new);
-            const uint32_t off = (r >> 7) * (kTileSlots * D) + ktile_off(r & 127, dim0, D);
-            float y[EPL], q[EPL];
-            decode_codes<EPL>(load_codes<EPL>(sc + off), y);
+            const float mult = __fdiv_rn(gsk[r], s_new);
+            const float2 m2 = make_float2(mult, mult);
+            float2 v[8];
+            decode16(raw[b], v);
+            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < EPL / 2; ++j) {
-                float a, b;
-                rotate_pair(y[2 * j], y[2 * j + 1], cs_c[j], cs_s[j], a, b);
-                q[2 * j] = a * mult;
-                q[2 * j + 1] = b * mult;
+            for (int q = 0; q < 4; ++q) {
+                const float2 x0 = mul2(rotate2(v[2 * q], cs[2 * q], sc[2 * q]), m2);
+                const float2 x1 = mul2(rotate2(v[2 * q + 1], cs[2 * q + 1], sc[2 * q + 1]), m2);
+                w[q] = e4m3x2(x0.x, x0.y) | (e4m3x2(x1.x, x1.y) << 16);
             }
-            store_codes<EPL>(gkc + off, encode_codes<EPL>(q));
-            if (lane == 0) gsk[r] = s_new;
+            *reinterpret_cast<uint4*>(chunk_addr(r)) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (chunk == 0) gsk[r] = s_new;
         }
     }
 }
 
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status) {
     const int tpc = (p.T + kRotCluster - 1) / kRotCluster;
-    const RotSmem L = rot_smem(tpc, D, p.Cpad);
+    const size_t smem = static_cast<size_t>(p.Cpad) * 4;
     dim3 grid(kRotCluster, p.H, layers);
     cudaError_t e;
     if (D == 128) {
-        e = cudaFuncSetAttribute(rotate_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        e = cudaFuncSetAttribute(rotate_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        rotate_kernel<128><<<grid, kRotThreads, L.total, s>>>(p, tpc, status);
+        rotate_kernel<128><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
     } else {
-        e = cudaFuncSetAttribute(rotate_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        e = cudaFuncSetAttribute(rotate_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        rotate_kernel<64><<<grid, kRotThreads, L.total, s>>>(p, tpc, status);
+        rotate_kernel<64><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
     }
     return cudaGetLastError();
 }

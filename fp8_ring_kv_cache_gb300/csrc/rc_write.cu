@@ -5,11 +5,12 @@
 // K1 rope_table_kernel: cos/sin of p * theta_i for the n positions of a write,
 //    angle formed in fp64 so large positions keep full accuracy.
 // K2 write_kernel: one thread-block cluster of 8 CTAs per head.  Each CTA
-//    loads its share of the n tokens (bf16 K and V), rotates K, and reduces the
-//    head's amax for K and for V across the cluster through distributed
-//    shared memory; then every element becomes the E4M3 code of fl32(x / s)
-//    with s = fl32(amax / 448) and is scattered into its ring slot: K rows into
-//    the swizzled K tile, V through a shared-memory transpose into the Vt tile.
+//    bulk-copies its share of the n tokens (one 256-byte bf16 K row and V row
+//    per token) into shared memory, rotates K, and reduces the head's amax for
+//    K and for V across the cluster through distributed shared memory; then
+//    every element becomes the E4M3 code of fl32(x / s) with
+//    s = fl32(amax / 448) and is scattered into its ring slot: K rows into the
+//    swizzled K tile, V through a shared-memory transpose into the Vt tile.
 //    HBM traffic is one read of K and V and one write of the codes.
 #include "rc_device.cuh"
 #include "rc_internal.h"
@@ -37,19 +38,36 @@ cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t s) {
 constexpr int kWriteCluster = 8;
 constexpr int kWriteWarps = 8;
 constexpr int kWriteThreads = kWriteWarps * 32;
-constexpr int kWriteTPW = 12;  // tokens per warp per batch
-constexpr int kWriteBatch = kWriteWarps * kWriteTPW;
+constexpr int kWriteTB = 96;  // tokens staged in shared memory per batch
+
+template <int D>
+struct WriteSmem {
+    static constexpr int kVRow = D + 4;  // padded V staging row (consecutive tokens hit different banks)
+    static constexpr uint32_t kK = 0;                                   // bf16 [TB][D]
+    static constexpr uint32_t kV = kK + kWriteTB * D * 2;               // bf16 [TB][D]
+    static constexpr uint32_t kStage = kV + kWriteTB * D * 2;           // u8 [TB][kVRow]
+    static constexpr uint32_t kSlot = kStage + kWriteTB * kVRow;        // int32 [TB]
+    static constexpr uint32_t kBar = (kSlot + kWriteTB * 4 + 7) / 8 * 8;
+    static constexpr uint32_t kTotal = kBar + 16;
+};
 
 template <int D>
 __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteThreads)
     write_kernel(WriteParams p) {
+    using S = WriteSmem<D>;
     constexpr int EPL = D / 32;       // elements per lane (4 or 2)
     constexpr int HALF = D / 2;
-    constexpr int VROW = D + 4;       // padded staging row (bank spread)
-    __shared__ __align__(16) uint8_t vstage[kWriteBatch * VROW];
+    constexpr uint32_t ROWB = D * 2;  // bytes of one bf16 head row
+    extern __shared__ __align__(128) uint8_t smem[];
+    __nv_bfloat16* kbuf = reinterpret_cast<__nv_bfloat16*>(smem + S::kK);
+    __nv_bfloat16* vbuf = reinterpret_cast<__nv_bfloat16*>(smem + S::kV);
+    uint8_t* vstage = smem + S::kStage;
+    int32_t* sslot = reinterpret_cast<int32_t*>(smem + S::kSlot);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kBar);
     __shared__ float red[2][kWriteWarps];
     __shared__ float cta_amax[2];
     __shared__ float scales[2];
+    __shared__ uint32_t abort_flag;
 
     const int h = blockIdx.y;
     const int crank = blockIdx.x;     // the cluster spans blockIdx.x
@@ -57,63 +75,99 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     const int tpc = (p.n + kWriteCluster - 1) / kWriteCluster;
     const int t0 = min(p.n, crank * tpc);
     const int t1 = min(p.n, t0 + tpc);
-    const int nbatch = (t1 - t0 + kWriteBatch - 1) / kWriteBatch;
+    const int nbatch = (t1 - t0 + kWriteTB - 1) / kWriteTB;
     const int dim0 = lane * EPL;
+    AbortState ab{&abort_flag, p.status};
 
-    float kreg[kWriteTPW][EPL];
-    float vreg[kWriteTPW][EPL];
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
 
-    auto load_batch = [&](int b, bool first_pass, float& amk, float& amv) {
-#pragma unroll
-        for (int i = 0; i < kWriteTPW; ++i) {
-            const int t = t0 + b * kWriteBatch + i * kWriteWarps + warp;
-            if (t < t1) {
-                const size_t src = (static_cast<size_t>(t) * p.H + h) * D + dim0;
-                __nv_bfloat16 kb[EPL], vb[EPL];
-                if constexpr (EPL == 4) {
-                    *reinterpret_cast<uint2*>(kb) = *reinterpret_cast<const uint2*>(p.K + src);
-                    *reinterpret_cast<uint2*>(vb) = *reinterpret_cast<const uint2*>(p.V + src);
-                } else {
-                    *reinterpret_cast<uint32_t*>(kb) = *reinterpret_cast<const uint32_t*>(p.K + src);
-                    *reinterpret_cast<uint32_t*>(vb) = *reinterpret_cast<const uint32_t*>(p.V + src);
-                }
-                float2 cs[EPL / 2];
-#pragma unroll
-                for (int j = 0; j < EPL / 2; ++j) cs[j] = p.rope[static_cast<size_t>(t) * HALF + dim0 / 2 + j];
-#pragma unroll
-                for (int j = 0; j < EPL / 2; ++j) {
-                    rotate_pair(__bfloat162float(kb[2 * j]), __bfloat162float(kb[2 * j + 1]), cs[j].x, cs[j].y,
-                                kreg[i][2 * j], kreg[i][2 * j + 1]);
-                }
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    vreg[i][e] = __bfloat162float(vb[e]);
-                    amk = fmaxf(amk, fabsf(kreg[i][e]));
-                    amv = fmaxf(amv, fabsf(vreg[i][e]));
-                }
-                if (first_pass && p.kraw != nullptr) {
-                    // read-time ablation store: the unrotated bf16 row and its angles
-                    const int64_t pos = p.pos ? p.pos[t] : p.p0 + t;
-                    const int slot = static_cast<int>(floormod64(pos - p.delta_total, p.C));
-                    const size_t dst = (static_cast<size_t>(h) * p.Cpad + slot) * D + dim0;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) {
-                        p.kraw[dst + e] = kb[e];
-                        p.vraw[dst + e] = vb[e];
-                    }
-                    if (h == 0) {
-#pragma unroll
-                        for (int j = 0; j < EPL / 2; ++j)
-                            p.slot_rope[static_cast<size_t>(slot) * HALF + dim0 / 2 + j] = cs[j];
-                    }
-                }
+    // slot of token t: floormod(pos - delta_total, C); an arithmetic run starts at slot0
+    auto slot_of = [&](int t) -> int {
+        if (p.pos == nullptr) {
+            const int s = p.slot0 + t;  // t < n <= C
+            return s >= p.C ? s - p.C : s;
+        }
+        return static_cast<int>(floormod64(p.pos[t] - p.delta_total, p.C));
+    };
+    // bring tokens [tb, tb + cnt) of this head into shared memory: two bulk
+    // copies (K row, V row) per token, all in flight on one mbarrier phase
+    uint32_t phase = 0;
+    auto stage_batch = [&](int tb, int cnt) -> bool {
+        if (warp == 0) {
+            if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 2 * ROWB);
+            __syncwarp();
+            for (int tl = lane; tl < cnt; tl += 32) {
+                const size_t src = (static_cast<size_t>(tb + tl) * p.H + h) * D;
+                bulk_g2s(kbuf + tl * D, p.K + src, ROWB, bar);
+                bulk_g2s(vbuf + tl * D, p.V + src, ROWB, bar);
             }
         }
+        const bool ok = mbar_wait(bar, phase & 1, ab, kDevTimeoutLoader);
+        ++phase;
+        return ok;
+    };
+    // token tl of the staged batch: K rotated at its position (EPL values of this lane) and V
+    auto row = [&](int tb, int tl, float (&k)[EPL], float (&v)[EPL]) {
+        __nv_bfloat16 kb[EPL], vb[EPL];
+        if constexpr (EPL == 4) {
+            *reinterpret_cast<uint2*>(kb) = *reinterpret_cast<const uint2*>(kbuf + tl * D + dim0);
+            *reinterpret_cast<uint2*>(vb) = *reinterpret_cast<const uint2*>(vbuf + tl * D + dim0);
+        } else {
+            *reinterpret_cast<uint32_t*>(kb) = *reinterpret_cast<const uint32_t*>(kbuf + tl * D + dim0);
+            *reinterpret_cast<uint32_t*>(vb) = *reinterpret_cast<const uint32_t*>(vbuf + tl * D + dim0);
+        }
+        const float2* rr = p.rope + static_cast<size_t>(tb + tl) * HALF + dim0 / 2;
+#pragma unroll
+        for (int j = 0; j < EPL / 2; ++j) {
+            const float2 cs = rr[j];
+            rotate_pair(__bfloat162float(kb[2 * j]), __bfloat162float(kb[2 * j + 1]), cs.x, cs.y, k[2 * j],
+                        k[2 * j + 1]);
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[e] = __bfloat162float(vb[e]);
     };
 
     // ---- phase 1: per-head amax of rotated K and of V over this CTA's tokens
     float amk = 0.f, amv = 0.f;
-    for (int b = 0; b < nbatch; ++b) load_batch(b, true, amk, amv);
+    bool ok = true;
+    for (int b = 0; b < nbatch; ++b) {
+        const int tb = t0 + b * kWriteTB;
+        const int cnt = min(kWriteTB, t1 - tb);
+        ok = stage_batch(tb, cnt) && ok;
+        if (ok) {
+            for (int tl = warp; tl < cnt; tl += kWriteWarps) {
+                float k[EPL], v[EPL];
+                row(tb, tl, k, v);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    amk = fmaxf(amk, fabsf(k[e]));
+                    amv = fmaxf(amv, fabsf(v[e]));
+                }
+                if (p.kraw != nullptr) {
+                    // read-time ablation store: the unrotated bf16 row and its angles
+                    const int slot = slot_of(tb + tl);
+                    const size_t dst = (static_cast<size_t>(h) * p.Cpad + slot) * D + dim0;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) {
+                        p.kraw[dst + e] = kbuf[tl * D + dim0 + e];
+                        p.vraw[dst + e] = vbuf[tl * D + dim0 + e];
+                    }
+                    if (h == 0) {
+#pragma unroll
+                        for (int j = 0; j < EPL / 2; ++j)
+                            p.slot_rope[static_cast<size_t>(slot) * HALF + dim0 / 2 + j] =
+                                p.rope[static_cast<size_t>(tb + tl) * HALF + dim0 / 2 + j];
+                    }
+                }
+            }
+        }
+        __syncthreads();  // the next batch overwrites the staging buffers
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         amk = fmaxf(amk, __shfl_xor_sync(0xffffffffu, amk, o));
@@ -139,66 +193,75 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     }
     cluster_sync();  // no CTA touches another's shared memory after this point
     const float sK = scales[0], sV = scales[1];
+    const float rK = __frcp_rn(sK), rV = __frcp_rn(sV);
 
-    // ---- phase 2: quantise and scatter
-    for (int b = 0; b < nbatch; ++b) {
+    // ---- phase 2: quantise and scatter (a single batch is still staged)
+    for (int b = 0; b < nbatch && ok; ++b) {
+        const int tb = t0 + b * kWriteTB;
+        const int cnt = min(kWriteTB, t1 - tb);
         if (nbatch > 1) {
-            float dk = 0.f, dv = 0.f;
-            load_batch(b, false, dk, dv);
+            ok = stage_batch(tb, cnt);
+            if (!ok) break;
         }
-        const int tb = t0 + b * kWriteBatch;
-        const int cnt = min(kWriteBatch, t1 - tb);
+        for (int tl = warp; tl < cnt; tl += kWriteWarps) {
+            float k[EPL], v[EPL];
+            row(tb, tl, k, v);
+            const int slot = slot_of(tb + tl);
+            if (lane == 0) sslot[tl] = slot;
+            uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
+            float qk[EPL], qv[EPL];
 #pragma unroll
-        for (int i = 0; i < kWriteTPW; ++i) {
-            const int tl = i * kWriteWarps + warp;
-            const int t = tb + tl;
-            if (tl < cnt) {
-                const int64_t pos = p.pos ? p.pos[t] : p.p0 + t;
-                const int slot = static_cast<int>(floormod64(pos - p.delta_total, p.C));
-                const int tile = slot >> 7, row = slot & 127;
-                uint8_t* krow = p.kc + static_cast<size_t>(h * p.T + tile) * (kTileSlots * D);
-                if constexpr (EPL == 4) {
-                    const uint32_t lo = e4m3x2(__fdiv_rn(kreg[i][0], sK), __fdiv_rn(kreg[i][1], sK));
-                    const uint32_t hi = e4m3x2(__fdiv_rn(kreg[i][2], sK), __fdiv_rn(kreg[i][3], sK));
-                    *reinterpret_cast<uint32_t*>(krow + ktile_off(row, dim0, D)) = lo | (hi << 16);
-                    const uint32_t vlo = e4m3x2(__fdiv_rn(vreg[i][0], sV), __fdiv_rn(vreg[i][1], sV));
-                    const uint32_t vhi = e4m3x2(__fdiv_rn(vreg[i][2], sV), __fdiv_rn(vreg[i][3], sV));
-                    *reinterpret_cast<uint32_t*>(vstage + tl * VROW + dim0) = vlo | (vhi << 16);
-                } else {
-                    const uint32_t k2 = e4m3x2(__fdiv_rn(kreg[i][0], sK), __fdiv_rn(kreg[i][1], sK));
-                    *reinterpret_cast<uint16_t*>(krow + ktile_off(row, dim0, D)) = static_cast<uint16_t>(k2);
-                    const uint32_t v2 = e4m3x2(__fdiv_rn(vreg[i][0], sV), __fdiv_rn(vreg[i][1], sV));
-                    *reinterpret_cast<uint16_t*>(vstage + tl * VROW + dim0) = static_cast<uint16_t>(v2);
-                }
-                if (lane == 0) {
-                    p.sk[static_cast<size_t>(h) * p.Cpad + slot] = sK;
-                    p.sv[static_cast<size_t>(h) * p.Cpad + slot] = sV;
-                    if (h == 0) p.grp[slot] = p.group;
-                }
+            for (int e = 0; e < EPL; ++e) {
+                qk[e] = div_by_scale(k[e], sK, rK);
+                qv[e] = div_by_scale(v[e], sV, rV);
+            }
+            if constexpr (EPL == 4) {
+                *reinterpret_cast<uint32_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
+                    e4m3x2(qk[0], qk[1]) | (e4m3x2(qk[2], qk[3]) << 16);
+                *reinterpret_cast<uint32_t*>(vstage + tl * S::kVRow + dim0) =
+                    e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
+            } else {
+                *reinterpret_cast<uint16_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
+                    static_cast<uint16_t>(e4m3x2(qk[0], qk[1]));
+                *reinterpret_cast<uint16_t*>(vstage + tl * S::kVRow + dim0) =
+                    static_cast<uint16_t>(e4m3x2(qv[0], qv[1]));
+            }
+            if (lane == 0) {
+                p.sk[static_cast<size_t>(h) * p.Cpad + slot] = sK;
+                p.sv[static_cast<size_t>(h) * p.Cpad + slot] = sV;
+                if (h == 0) p.grp[slot] = p.group;
             }
         }
         __syncthreads();
-        // V transposed: consecutive threads take consecutive tokens of one dim row
-        for (int idx = threadIdx.x; idx < D * cnt; idx += kWriteThreads) {
-            const int d = idx / cnt;
-            const int tl = idx - d * cnt;
-            const int t = tb + tl;
-            const int64_t pos = p.pos ? p.pos[t] : p.p0 + t;
-            const int slot = static_cast<int>(floormod64(pos - p.delta_total, p.C));
-            uint8_t* vtile = p.vt + static_cast<size_t>(h * p.T + (slot >> 7)) * (D * kTileSlots);
-            vtile[vtile_off(d, slot & 127)] = vstage[tl * VROW + d];
+        // V transposed: a warp takes one dim row, its lanes consecutive tokens
+        uint8_t* vhead = p.vt + static_cast<size_t>(h) * p.T * (D * kTileSlots);
+        for (int d = warp; d < D; d += kWriteWarps) {
+            for (int tl = lane; tl < cnt; tl += 32) {
+                const int slot = sslot[tl];
+                vhead[static_cast<size_t>(slot >> 7) * (D * kTileSlots) + vtile_off(d, slot & 127)] =
+                    vstage[tl * S::kVRow + d];
+            }
         }
         __syncthreads();
     }
 }
 
-cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s) {
+template <int D>
+static cudaError_t launch_write_d(const WriteParams& p, cudaStream_t s) {
+    static bool configured = false;
+    constexpr uint32_t smem = WriteSmem<D>::kTotal;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(write_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
     dim3 grid(kWriteCluster, p.H);
-    if (D == 128)
-        write_kernel<128><<<grid, kWriteThreads, 0, s>>>(p);
-    else
-        write_kernel<64><<<grid, kWriteThreads, 0, s>>>(p);
+    write_kernel<D><<<grid, kWriteThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s) {
+    return (D == 128) ? launch_write_d<128>(p, s) : launch_write_d<64>(p, s);
 }
 
 }  // namespace rc

@@ -20,8 +20,9 @@
  *     RC_ERR_CUDA from a later call, or from rc_cache_sync.  No C++ exception
  *     crosses this boundary.
  *   - Device pointers are plain CUDA device addresses (for example a torch
- *     tensor's data_ptr()).  The caller keeps them alive until the work on
- *     `stream` that reads or writes them has finished.
+ *     tensor's data_ptr()), 16-byte aligned (RC_ERR_ARG otherwise).  The
+ *     caller keeps them alive until the work on `stream` that reads or
+ *     writes them has finished.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls on one handle must be issued on one stream, or ordered
  *     by the caller; a handle is not thread-safe.
@@ -129,9 +130,11 @@ int rc_attend(rc_cache *h, int layer, const void *Q_bf16, float *out_f32, int n,
  * com batch size 1": RoPE and FP8 quantisation of the WHOLE cache redone in
  * every attention call).  Rebuilds this layer's FP8 ring from the unrotated
  * bf16 store into a scratch ring, then runs the same attention kernel on it.
- * Requires RC_F_READTIME_ABLATION, else RC_ERR_STATE.  The result equals
- * rc_attend's as long as no delta rotation has requantised the write-time
- * ring.
+ * Requires RC_F_READTIME_ABLATION, else RC_ERR_STATE.  The read-time ring
+ * quantises each head with ONE scale over all occupied slots (per K and V),
+ * so its codes differ from the write-time ring's wherever that ring holds
+ * several write groups with different scales; the rotated keys before
+ * quantisation are the same.
  */
 int rc_attend_readtime(rc_cache *h, int layer, const void *Q_bf16, float *out_f32,
                        int n, void *stream);
