@@ -7,16 +7,17 @@
 //    one fp32 scale sq = fl32(amax / 448) per row, and three E4M3 pieces
 //    (hi + mid + lo, 12 significant bits) of q / sq, written straight into the
 //    swizzled shared-memory image the attention kernel's A operand needs.
-//    Extra blocks take each head's largest V scale.
+//    The first H blocks take each head's largest V scale.
 // K4 attn_kernel: one CTA = one head x 256 query rows (two 128-row M tiles),
 //    448 threads:
 //   warp 0        loader: bulk copies of the prepared query pieces, then one
-//                 bulk copy per K tile, Vt tile and scale vectors per 128-slot
-//                 KV tile, double-buffered (mbarrier + complete_tx)
+//                 bulk copy per K tile and scale vectors per 128-slot KV tile,
+//                 double-buffered (mbarrier + complete_tx)
 //   warp 1        MMA issuer (one lane) and TMEM owner (512 columns)
 //   warps 2..5    softmax group 0 (rows 0..127; one row per thread / TMEM lane)
 //   warps 6..9    softmax group 1 (rows 128..255)
-//   warps 10..13  converter: Vt E4M3 tile -> fp16 tile (exact), 128-byte swizzle
+//   warps 10..11  converter: Vt E4M3 tile (read from global memory half a
+//                 tile ahead) -> fp16 tile (exact), 128-byte swizzle, two buffers
 // Per KV tile j and M tile i:
 //   S_i = Q_i K_j^T on tcgen05 kind::f8f6f4: the three Q pieces accumulate into
 //         one fp32 TMEM tile, so the score error stays inside the tolerance.
@@ -33,13 +34,16 @@
 
 namespace rc {
 
-constexpr int kAttnWarps = 14;
+// 12 warps: each of the four schedulers of an SM runs one softmax warp of
+// each M tile and one of {loader, MMA, converter, converter}, and the
+// register file allows 168 registers a thread.
+constexpr int kAttnWarps = 12;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kQPieces = 3;
 constexpr int kStages = 2;
 constexpr int kMTile = 128;
 constexpr int kRowsPerCta = 2 * kMTile;
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpSm0 = 2, kWarpCvt = 10;
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpSm0 = 2, kWarpCvt = 10, kCvtWarps = 2;
 constexpr uint32_t kTmemCols = 512;
 // The converted V tile holds code / 256 (the E4M3 bits placed in an fp16), so
 // O accumulates P V / 256; the epilogue multiplies the 256 back in.
@@ -47,16 +51,16 @@ constexpr float kV16Scale = 256.f;
 
 // barrier indices
 enum : int {
-    B_KV_FULL = 0,   // [2]
-    B_KV_EMPTY = 2,  // [2]
-    B_V16_FULL = 4,
-    B_V16_EMPTY = 5,
-    B_S_FULL = 6,    // [2]
-    B_P_FULL = 8,    // [2]
-    B_O_DONE = 10,   // [2]
-    B_DRAIN = 12,
-    B_Q_FULL = 13,
-    B_COUNT = 14
+    B_KV_FULL = 0,     // [kStages]
+    B_KV_EMPTY = 3,    // [kStages]
+    B_V16_FULL = 6,    // [2]
+    B_V16_EMPTY = 8,   // [2]
+    B_S_FULL = 10,     // [2]
+    B_P_FULL = 12,     // [2]
+    B_O_DONE = 14,     // [2]
+    B_DRAIN = 16,
+    B_Q_FULL = 17,
+    B_COUNT = 18
 };
 
 template <int D>
@@ -64,13 +68,14 @@ struct AttnLayout {
     static constexpr uint32_t kTile = kTileSlots * D;  // bytes of a K tile or a Vt tile
     static constexpr uint32_t kQ = 0;                   // [piece][mtile][128][D] E4M3
     static constexpr uint32_t kQBytes = kQPieces * 2 * kMTile * D;
-    static constexpr uint32_t kStage0 = kQBytes;        // K8, V8, sk[128], sv[128], grp[128]
-    static constexpr uint32_t kStageBytes = ((2 * kTile + 3 * 512) + 1023) / 1024 * 1024;
-    static constexpr uint32_t kV16 = kStage0 + kStages * kStageBytes;  // [2 halves][D][128 B] fp16
-    static constexpr uint32_t kV16Bytes = 2 * D * 128;
+    static constexpr uint32_t kStage0 = kQBytes;        // K8, sk[128], sv[128], grp[128]
+    static constexpr uint32_t kStageBytes = ((kTile + 3 * 512) + 1023) / 1024 * 1024;
+    static constexpr uint32_t kV16 = kStage0 + kStages * kStageBytes;  // 2 x [2 halves][D][128 B] fp16
+    static constexpr uint32_t kV16One = 2 * D * 128;
+    static constexpr uint32_t kV16Bytes = 2 * kV16One;
     static constexpr uint32_t kSq = kV16 + kV16Bytes;  // fp32 [256] row scales, then svmax (16 B)
     static constexpr uint32_t kBar = kSq + 2 * kMTile * 4 + 16;
-    static constexpr uint32_t kMisc = kBar + 8 * 16;
+    static constexpr uint32_t kMisc = kBar + 8 * B_COUNT;
     static constexpr uint32_t kTotal = kMisc + 64;
     static constexpr uint32_t kAlloc = kTotal + 1024;  // room to align the base to 1024
 };
@@ -84,12 +89,14 @@ __global__ void __launch_bounds__(kPrepWarps * 32) q_prep_kernel(QPrepParams p) 
     constexpr int EPL = D / 32;
     const int lane = threadIdx.x & 31;
     const int rows = p.nmt * kMTile;
-    const int nrb = (p.H * rows + kPrepWarps - 1) / kPrepWarps;
-    if (static_cast<int>(blockIdx.x) >= nrb) {
-        // the head's largest V scale (empty slots hold 0)
-        const int h = blockIdx.x - nrb;
+    if (static_cast<int>(blockIdx.x) < p.H) {
+        // the head's largest V scale (empty slots hold 0); first in the grid so
+        // these longer blocks start early, eight loads in flight per thread
+        const int h = blockIdx.x;
+        const float* svh = p.sv + static_cast<size_t>(h) * p.Cpad;
         float m = 0.f;
-        for (int i = threadIdx.x; i < p.C; i += kPrepWarps * 32) m = fmaxf(m, p.sv[static_cast<size_t>(h) * p.Cpad + i]);
+#pragma unroll 8
+        for (int i = threadIdx.x; i < p.C; i += kPrepWarps * 32) m = fmaxf(m, svh[i]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         __shared__ float red[kPrepWarps];
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) q_prep_kernel(QPrepParams p) 
         }
         return;
     }
-    const int w = blockIdx.x * kPrepWarps + (threadIdx.x >> 5);
+    const int w = (blockIdx.x - p.H) * kPrepWarps + (threadIdx.x >> 5);
     if (w >= p.H * rows) return;
     const int h = w / rows, row = w - h * rows;
     const int dim0 = lane * EPL;
@@ -206,11 +213,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[B_KV_FULL + s], 1);
-            mbar_init(&bars[B_KV_EMPTY + s], 1 + 4 + 8);
+            mbar_init(&bars[B_KV_EMPTY + s], 1 + 8);  // the MMA warp and the 8 softmax warps
         }
-        mbar_init(&bars[B_V16_FULL], 4);
-        mbar_init(&bars[B_V16_EMPTY], 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_V16_FULL + i], kCvtWarps);  // the converter warps
+            mbar_init(&bars[B_V16_EMPTY + i], 1);
             mbar_init(&bars[B_S_FULL + i], 1);
             mbar_init(&bars[B_P_FULL + i], 4);
             mbar_init(&bars[B_O_DONE + i], 1);
@@ -246,19 +253,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             bulk_g2s(smem + Lay::kSq, p.qs + static_cast<size_t>(h) * p.nmt * kMTile + mt0 * kMTile, 2 * kMTile * 4,
                      qf);
             bulk_g2s(smem + Lay::kSq + 2 * kMTile * 4, p.svm + h * 4, 16, qf);
-            const uint32_t bytes = 2 * Lay::kTile + 1024 + (p.masked ? 512 : 0);
+            const uint32_t bytes = Lay::kTile + 1024 + (p.masked ? 512 : 0);
             for (int j = 0; j < T; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&bars[B_KV_EMPTY + s], ((j >> 1) & 1) ^ 1, ab, kDevTimeoutLoader)) break;
+                const int s = j % kStages;
+                if (!mbar_wait(&bars[B_KV_EMPTY + s], ((j / kStages) & 1) ^ 1, ab, kDevTimeoutLoader)) break;
                 uint8_t* st = stage_ptr(s);
                 uint64_t* full = &bars[B_KV_FULL + s];
                 mbar_arrive_expect_tx(full, bytes);
                 bulk_g2s(st, p.kc + (static_cast<size_t>(h) * T + j) * Lay::kTile, Lay::kTile, full);
-                bulk_g2s(st + Lay::kTile, p.vt + (static_cast<size_t>(h) * T + j) * Lay::kTile, Lay::kTile, full);
-                bulk_g2s(st + 2 * Lay::kTile, p.sk + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
-                bulk_g2s(st + 2 * Lay::kTile + 512, p.sv + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512,
-                         full);
-                if (p.masked) bulk_g2s(st + 2 * Lay::kTile + 1024, p.grp + j * kTileSlots, 512, full);
+                bulk_g2s(st + Lay::kTile, p.sk + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
+                bulk_g2s(st + Lay::kTile + 512, p.sv + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
+                if (p.masked) bulk_g2s(st + Lay::kTile + 1024, p.grp + j * kTileSlots, 512, full);
             }
             if (*ab.flag) {
                 // leave no copy in flight: wait (bounded) for the query copies and
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 for (int s = 0; s < kStages && s < T; ++s) {
                     const int last = ((T - 1 - s) / kStages) * kStages + s;
                     t0 = global_timer_ns();
-                    while (!mbar_try_wait(&bars[B_KV_FULL + s], (last >> 1) & 1) &&
+                    while (!mbar_try_wait(&bars[B_KV_FULL + s], (last / kStages) & 1) &&
                            global_timer_ns() - t0 < 100000000ull) {
                     }
                 }
@@ -294,29 +299,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                         mma_f8_ss(d_tmem, a, b, idesc_qk, (pc | k) != 0);
                     }
             };
-            auto issue_pv = [&](int i, bool acc) {
+            auto issue_pv = [&](int i, int jt, bool acc) {
                 const uint32_t d_tmem = tmem + 256u + static_cast<uint32_t>(D) * i;
                 const uint32_t a_tmem = tmem + 128u * i;
+                const uint32_t vb = v16_base + (jt & 1) * Lay::kV16One;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t b = smem_desc(v16_base + (kk >> 2) * (D * 128) + (kk & 3) * 32, 16, 1024, 2);
+                    const uint64_t b = smem_desc(vb + (kk >> 2) * (D * 128) + (kk & 3) * 32, 16, 1024, 2);
                     mma_f16_ts(d_tmem, a_tmem + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
             bool ok = mbar_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutMma);
             for (int j = 0; j < T && ok; ++j) {
-                const int s = j & 1;
-                ok = mbar_wait(&bars[B_KV_FULL + s], (j >> 1) & 1, ab, kDevTimeoutMma);
+                const int s = j % kStages;
+                ok = mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutMma);
                 if (!ok) break;
                 tc_fence_after();
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (j > 0) {
                         ok = mbar_wait(&bars[B_P_FULL + i], (j - 1) & 1, ab, kDevTimeoutMma);
-                        if (ok && i == 0) ok = mbar_wait(&bars[B_V16_FULL], (j - 1) & 1, ab, kDevTimeoutMma);
+                        if (ok && i == 0)
+                            ok = mbar_wait(&bars[B_V16_FULL + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kDevTimeoutMma);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(i, j - 1 > 0);
-                        if (i == 1) mma_commit(&bars[B_V16_EMPTY]);
+                        issue_pv(i, j - 1, j - 1 > 0);
+                        if (i == 1) mma_commit(&bars[B_V16_EMPTY + ((j - 1) & 1)]);
                     }
                     issue_qk(i, s);
                     mma_commit(&bars[B_S_FULL + i]);
@@ -325,10 +332,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             }
             for (int i = 0; i < 2 && ok; ++i) {
                 ok = mbar_wait(&bars[B_P_FULL + i], (T - 1) & 1, ab, kDevTimeoutMma);
-                if (ok && i == 0) ok = mbar_wait(&bars[B_V16_FULL], (T - 1) & 1, ab, kDevTimeoutMma);
+                if (ok && i == 0)
+                    ok = mbar_wait(&bars[B_V16_FULL + ((T - 1) & 1)], ((T - 1) >> 1) & 1, ab, kDevTimeoutMma);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(i, T - 1 > 0);
+                issue_pv(i, T - 1, T - 1 > 0);
                 mma_commit(&bars[B_O_DONE + i]);
             }
             // every MMA has finished before the tensor memory is released
@@ -358,120 +366,189 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         const float2 a2 = make_float2(a, a);
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < T && ok; ++j) {
-            const int s = j & 1;
-            ok = warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax);
-            if (ok) ok = warp_wait(&bars[B_KV_FULL + s], (j >> 1) & 1, ab, kDevTimeoutSoftmax);
+            const int s = j % kStages;
+            // the tile's scales land with its K tile, before its scores: read them first
+            ok = warp_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutSoftmax);
             if (!ok) break;
-            tc_fence_after();
             const uint8_t* st = stage_ptr(s);
-            const float* ssk = reinterpret_cast<const float*>(st + 2 * Lay::kTile);
+            const float* ssk = reinterpret_cast<const float*>(st + Lay::kTile);
             const float* ssv = ssk + kTileSlots;
             const int32_t* sgrp = reinterpret_cast<const int32_t*>(ssv + kTileSlots);
             const int nvalid = min(kTileSlots, p.C - j * kTileSlots);
             const bool full = (nvalid == kTileSlots) && !p.masked;
+            // one write group fills the tile: one K and one V scale, no per-column loads
+            const bool uni = (p.uniform[j >> 6] >> (j & 63)) & 1ull;
+            const float cu = uni ? ssk[0] * a : 0.f;
+            const float lsv0 = uni ? lg2_approx(ssv[0]) : 0.f;
+            const float isv0 = uni ? ex2(-lsv0) : 1.f;
             auto valid = [&](int col) { return col < nvalid && (!p.masked || sgrp[col] >= 0); };
+            ok = warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax);
+            if (!ok) break;
+            tc_fence_after();
 
-            // pass A: the tile's largest score (in units of a).  32-column TMEM
-            // loads are double-buffered: the next chunk loads while this one is used.
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            auto max_chunk = [&](const uint32_t (&v)[32], int c) {
-                if (full) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
-                        const float2 x0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                               make_float2(s4.x, s4.y));
-                        const float2 x1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                               make_float2(s4.z, s4.w));
-                        mx[(k >> 2) & 1] = max3(mx[(k >> 2) & 1], x0.x, x0.y);
-                        mx[2 + ((k >> 2) & 1)] = max3(mx[2 + ((k >> 2) & 1)], x1.x, x1.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int col = 32 * c + k;
-                        if (valid(col)) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]) * ssk[col]);
-                    }
-                }
-            };
-            {
-                uint32_t va[32], vb[32];
-                tmem_ld32_async(s_tm, va);
-                tmem_wait_ld_dep(va);
-                tmem_ld32_async(s_tm + 32, vb);
-                max_chunk(va, 0);
-                tmem_wait_ld_dep(vb);
-                tmem_ld32_async(s_tm + 64, va);
-                max_chunk(vb, 1);
-                tmem_wait_ld_dep(va);
-                tmem_ld32_async(s_tm + 96, vb);
-                max_chunk(va, 2);
-                tmem_wait_ld_dep(vb);
-                max_chunk(vb, 3);
-            }
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
-            const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
-            const float m_new = bump ? fmaxf(m_run, m_tile) : m_run;
-            const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = bump ? ex2(m_run - m_fin) : 1.f;
-            const float msub = m_fin + lsv;
-            const float2 nm2 = make_float2(-msub, -msub);
-
-            // pass B: probabilities, row sum, fp16 P' written over the chunk's S
+            float m_new, alpha;
             float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            auto p_chunk = [&](const uint32_t (&v)[32], int c) {
-                uint32_t pk[16];
-                if (full) {
+            if (uni) {
+                // Uniform tile: the row's 128 scores come into registers with four
+                // TMEM loads and one wait; pass A (the tile max, one max3 tree) and
+                // pass B (the probabilities) both run from the registers.
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32_async(s_tm, v0);
+                tmem_ld32_async(s_tm + 32, v1);
+                tmem_ld32_async(s_tm + 64, v2);
+                tmem_ld32_async(s_tm + 96, v3);
+                tmem_wait_ld_dep(v0);
+                reg_fence(v1);
+                reg_fence(v2);
+                reg_fence(v3);
+                auto chunk_max = [](const uint32_t (&v)[32]) {
+                    float t[11];
+#pragma unroll
+                    for (int i = 0; i < 10; ++i)
+                        t[i] = max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                                    __uint_as_float(v[3 * i + 2]));
+                    t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+                    const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
+                    const float u2 = max3(t[6], t[7], t[8]), u3 = max3(t[9], t[10], u0);
+                    return max3(u1, u2, u3);
+                };
+                const float mxall = fmaxf(fmaxf(chunk_max(v0), chunk_max(v1)), fmaxf(chunk_max(v2), chunk_max(v3)));
+                const float m_tile = mxall * cu;
+                const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+                m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+                const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha = bump ? ex2(m_run - m_fin) : 1.f;
+                const float msub = m_fin + lsv;
+                // P' = exp2(S c - m - log2(max sv) + log2(sv)): the V scale rides in the exponent
+                const float2 cu2 = make_float2(cu, cu);
+                const float2 nmu2 = make_float2(lsv0 - msub, lsv0 - msub);
+                // all four chunks are computed before the stores, so the exp2 work
+                // runs back to back
+                auto p_chunk = [&](const uint32_t (&v)[32], uint32_t* pk) {
 #pragma unroll
                     for (int k = 0; k < 32; k += 4) {
-                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
-                        const float4 v4 = *reinterpret_cast<const float4*>(ssv + 32 * c + k);
-                        const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                                    make_float2(s4.x, s4.y)), a2, nm2);
-                        const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                                    make_float2(s4.z, s4.w)), a2, nm2);
-                        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-                        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-                        ls[0] = add2(ls[0], p0);
-                        ls[1] = add2(ls[1], p1);
-                        const float2 q0 = mul2(p0, make_float2(v4.x, v4.y));
-                        const float2 q1 = mul2(p1, make_float2(v4.z, v4.w));
+                        const float2 x0 = fma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), cu2, nmu2);
+                        const float2 x1 =
+                            fma2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), cu2, nmu2);
+                        const float2 q0 = make_float2(ex2(x0.x), ex2(x0.y));
+                        const float2 q1 = make_float2(ex2(x1.x), ex2(x1.y));
+                        ls[0] = add2(ls[0], q0);
+                        ls[1] = add2(ls[1], q1);
                         __half2 h0 = __floats2half2_rn(q0.x, q0.y);
                         __half2 h1 = __floats2half2_rn(q1.x, q1.y);
                         pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
                         pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
                     }
-                } else {
+                };
+                uint32_t pa[32], pb[32];
+                p_chunk(v0, pa);
+                p_chunk(v1, pa + 16);
+                p_chunk(v2, pb);
+                p_chunk(v3, pb + 16);
+                // P (128 slots as 64 fp16 pairs) goes to columns 0..63
+                tmem_st32(s_tm, pa);
+                tmem_st32(s_tm + 32, pb);
+            } else {
+                // Per-column scales (and, on a partial or masked tile, a validity
+                // test): pass A and pass B each read the scores from TMEM in
+                // 32-column chunks, the next chunk loading while one is used.
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                auto max_chunk = [&](const uint32_t (&v)[32], int c) {
+                    if (full) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
-                        const int c0 = 32 * c + k, c1 = c0 + 1;
-                        const float p0 = valid(c0) ? ex2(__fmaf_rn(__uint_as_float(v[k]) * ssk[c0], a, -msub)) : 0.f;
-                        const float p1 =
-                            valid(c1) ? ex2(__fmaf_rn(__uint_as_float(v[k + 1]) * ssk[c1], a, -msub)) : 0.f;
-                        ls[0].x += p0;
-                        ls[1].y += p1;
-                        __half2 hp = __floats2half2_rn(p0 * ssv[c0], p1 * ssv[c1]);
-                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
+                        for (int k = 0; k < 32; k += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
+                            const float2 x0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                                   make_float2(s4.x, s4.y));
+                            const float2 x1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                                   make_float2(s4.z, s4.w));
+                            mx[(k >> 2) & 1] = max3(mx[(k >> 2) & 1], x0.x, x0.y);
+                            mx[2 + ((k >> 2) & 1)] = max3(mx[2 + ((k >> 2) & 1)], x1.x, x1.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int col = 32 * c + k;
+                            if (valid(col)) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]) * ssk[col]);
+                        }
                     }
+                };
+                {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32_async(s_tm, va);
+                    tmem_wait_ld_dep(va);
+                    tmem_ld32_async(s_tm + 32, vb);
+                    max_chunk(va, 0);
+                    tmem_wait_ld_dep(vb);
+                    tmem_ld32_async(s_tm + 64, va);
+                    max_chunk(vb, 1);
+                    tmem_wait_ld_dep(va);
+                    tmem_ld32_async(s_tm + 96, vb);
+                    max_chunk(va, 2);
+                    tmem_wait_ld_dep(vb);
+                    max_chunk(vb, 3);
                 }
-                // P chunk c (32 slots as 16 fp16 pairs) goes to columns 16c..16c+15,
-                // which were read in chunks <= c
-                tmem_st16(s_tm + 16 * c, pk);
-            };
-            {
-                uint32_t va[32], vb[32];
-                tmem_ld32_async(s_tm, va);
-                tmem_wait_ld_dep(va);
-                tmem_ld32_async(s_tm + 32, vb);
-                p_chunk(va, 0);
-                tmem_wait_ld_dep(vb);
-                tmem_ld32_async(s_tm + 64, va);
-                p_chunk(vb, 1);
-                tmem_wait_ld_dep(va);
-                tmem_ld32_async(s_tm + 96, vb);
-                p_chunk(va, 2);
-                tmem_wait_ld_dep(vb);
-                p_chunk(vb, 3);
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
+                const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+                m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+                const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha = bump ? ex2(m_run - m_fin) : 1.f;
+                const float msub = m_fin + lsv;
+                const float2 nm2 = make_float2(-msub, -msub);
+                auto p_chunk = [&](const uint32_t (&v)[32], int c) {
+                    uint32_t pk[16];
+                    if (full) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
+                            const float4 v4 = *reinterpret_cast<const float4*>(ssv + 32 * c + k);
+                            const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                                        make_float2(s4.x, s4.y)), a2, nm2);
+                            const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                                        make_float2(s4.z, s4.w)), a2, nm2);
+                            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                            ls[0] = add2(ls[0], p0);
+                            ls[1] = add2(ls[1], p1);
+                            const float2 q0 = mul2(p0, make_float2(v4.x, v4.y));
+                            const float2 q1 = mul2(p1, make_float2(v4.z, v4.w));
+                            __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+                            __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+                            pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
+                            pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) {
+                            const int c0 = 32 * c + k, c1 = c0 + 1;
+                            const float p0 = valid(c0) ? ex2(__fmaf_rn(__uint_as_float(v[k]) * ssk[c0], a, -msub)) : 0.f;
+                            const float p1 =
+                                valid(c1) ? ex2(__fmaf_rn(__uint_as_float(v[k + 1]) * ssk[c1], a, -msub)) : 0.f;
+                            ls[0].x += p0;
+                            ls[1].y += p1;
+                            __half2 hp = __floats2half2_rn(p0 * (valid(c0) ? ssv[c0] : 0.f),
+                                                           p1 * (valid(c1) ? ssv[c1] : 0.f));
+                            pk[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
+                        }
+                    }
+                    // P chunk c goes to columns 16c..16c+15, which were read in chunks <= c
+                    tmem_st16(s_tm + 16 * c, pk);
+                };
+                {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32_async(s_tm, va);
+                    tmem_wait_ld_dep(va);
+                    tmem_ld32_async(s_tm + 32, vb);
+                    p_chunk(va, 0);
+                    tmem_wait_ld_dep(vb);
+                    tmem_ld32_async(s_tm + 64, va);
+                    p_chunk(vb, 1);
+                    tmem_wait_ld_dep(va);
+                    tmem_ld32_async(s_tm + 96, vb);
+                    p_chunk(va, 2);
+                    tmem_wait_ld_dep(vb);
+                    p_chunk(vb, 3);
+                }
             }
             tmem_st_wait();
             __syncwarp();
@@ -488,7 +565,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 }
                 tmem_st_wait();
             }
-            l_run = l_run * alpha + ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y));
+            // on uniform tiles the sum holds P' = P'' * 2^log2(sv): take the V scale back out
+            const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
+            l_run = l_run * alpha + lsum * isv0;
             m_run = m_new;
             tc_fence_before();
             __syncwarp();
@@ -515,35 +594,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         }
     } else {
         // ------------------------------------------------------------ V converter
+        // Reads each Vt tile straight from global memory (L2: the head's CTAs
+        // share it) in two halves, each fetched while the one before it is
+        // converted, and fills the two fp16 buffers alternately, so it runs
+        // ahead of the P.V MMAs.
+        constexpr int kCvtThreads = kCvtWarps * 32;
+        constexpr int kHalf = D * 8 / kCvtThreads / 2;  // 16-byte units a thread converts per half tile
         const int ct = tid - kWarpCvt * 32;
         uint8_t* v16 = smem + Lay::kV16;
-        for (int j = 0; j < T; ++j) {
-            const int s = j & 1;
-            bool ok = warp_wait(&bars[B_KV_FULL + s], (j >> 1) & 1, ab, kDevTimeoutConvert);
-            if (ok) ok = warp_wait(&bars[B_V16_EMPTY], (j & 1) ^ 1, ab, kDevTimeoutConvert);
-            if (!ok) break;
-            const uint8_t* v8 = stage_ptr(s) + Lay::kTile;
-#pragma unroll 4
-            for (int u = ct; u < D * 8; u += 128) {
+        const uint8_t* vhead = p.vt + static_cast<size_t>(h) * T * Lay::kTile;
+        auto fetch = [&](int hh, uint4 (&r)[kHalf]) {
+            const uint8_t* src = vhead + static_cast<size_t>(hh >> 1) * Lay::kTile;
+#pragma unroll
+            for (int k = 0; k < kHalf; ++k)
+                r[k] = __ldg(reinterpret_cast<const uint4*>(src + (ct + kCvtThreads * ((hh & 1) * kHalf + k)) * 16));
+        };
+        auto convert = [&](int hh, const uint4 (&r)[kHalf]) -> bool {
+            const int jt = hh >> 1, b = jt & 1;
+            if ((hh & 1) == 0 &&
+                !warp_wait(&bars[B_V16_EMPTY + b], ((jt >> 1) & 1) ^ 1, ab, kDevTimeoutConvert))
+                return false;
+            uint8_t* dstb = v16 + b * Lay::kV16One;
+#pragma unroll
+            for (int k = 0; k < kHalf; ++k) {
+                const int u = ct + kCvtThreads * ((hh & 1) * kHalf + k);
                 const int rr = u >> 3, cp = u & 7;
-                const uint4 raw = *reinterpret_cast<const uint4*>(v8 + rr * 128 + cp * 16);
                 const int c = cp ^ (rr & 7);  // logical 16-slot chunk
                 uint32_t o[8];
-                e4m3x4_to_f16x4_div256(raw.x, o[0], o[1]);
-                e4m3x4_to_f16x4_div256(raw.y, o[2], o[3]);
-                e4m3x4_to_f16x4_div256(raw.z, o[4], o[5]);
-                e4m3x4_to_f16x4_div256(raw.w, o[6], o[7]);
-                uint8_t* dst = v16 + (c >> 2) * (D * 128) + rr * 128;
+                e4m3x4_to_f16x4_div256(r[k].x, o[0], o[1]);
+                e4m3x4_to_f16x4_div256(r[k].y, o[2], o[3]);
+                e4m3x4_to_f16x4_div256(r[k].z, o[4], o[5]);
+                e4m3x4_to_f16x4_div256(r[k].w, o[6], o[7]);
+                uint8_t* dst = dstb + (c >> 2) * (D * 128) + rr * 128;
                 const int l0 = 2 * (c & 3);
                 *reinterpret_cast<uint4*>(dst + (((l0) ^ (rr & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4*>(dst + (((l0 + 1) ^ (rr & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_V16_FULL]);
-                mbar_arrive(&bars[B_KV_EMPTY + s]);
+            if (hh & 1) {
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_V16_FULL + b]);
             }
+            return true;
+        };
+        uint4 ra[kHalf], rb[kHalf];
+        const int nh = 2 * T;
+        if (nh > 0) fetch(0, ra);
+        for (int hh = 0; hh < nh; hh += 2) {
+            fetch(hh + 1, rb);
+            if (!convert(hh, ra)) break;
+            if (hh + 2 < nh) fetch(hh + 2, ra);
+            if (!convert(hh + 1, rb)) break;
         }
     }
 

@@ -6,6 +6,7 @@
 // em tempo real com batch size 1": the window advances without copies): token
 // at position p lives in slot floormod(p - delta_total, C).  A delta rotation
 // adds delta to every stored position and to delta_total, so no token moves.
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -72,6 +73,8 @@ struct rc_cache {
     std::vector<std::vector<int32_t>> refcnt, freelist;  // per layer
     std::vector<std::vector<int64_t>> last_pos;          // per layer
     std::vector<int> last_n, last_entry;
+    std::vector<std::array<uint64_t, 4>> uniform;  // per layer: tiles inside one write group
+    std::vector<char> uniform_dirty;
     std::vector<uint32_t> slot_mark;
     uint32_t mark = 0;
     std::vector<double> theta;
@@ -118,6 +121,22 @@ void free_all(rc_cache* h) {
         if (e.copied) cudaEventDestroy(e.copied);
     }
     delete h;
+}
+
+// Tiles whose 128 slots are all occupied by a single write group.
+void refresh_uniform(rc_cache* h, int layer) {
+    if (!h->uniform_dirty[layer]) return;
+    auto& m = h->uniform[layer];
+    m = {0, 0, 0, 0};
+    const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
+    for (int t = 0; t < h->T && t < 256; ++t) {
+        const int s0 = t * kTileSlots;
+        if (s0 + kTileSlots > h->C || g[s0] < 0) continue;
+        bool same = true;
+        for (int s = s0 + 1; s < s0 + kTileSlots && same; ++s) same = (g[s] == g[s0]);
+        if (same) m[t >> 6] |= 1ull << (t & 63);
+    }
+    h->uniform_dirty[layer] = 0;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -318,6 +337,8 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     for (auto& v : h->last_pos) v.reserve(h->max_write);
     h->last_n.assign(h->L, 0);
     h->last_entry.assign(h->L, -1);
+    h->uniform.assign(h->L, std::array<uint64_t, 4>{0, 0, 0, 0});
+    h->uniform_dirty.assign(h->L, 1);
     h->slot_mark.assign(h->C, 0);
     *out = h;
     return RC_OK;
@@ -407,6 +428,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     if (launch_write(wp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
     h->last_pos[layer].assign(positions, positions + n);
+    h->uniform_dirty[layer] = 1;
     h->last_n[layer] = n;
     h->last_entry[layer] = entry;
     h->next_gid += 1;
@@ -526,6 +548,21 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     ap.T = h->T;
     ap.Cpad = h->Cpad;
     ap.masked = (h->occupancy[layer] < h->C) ? 1 : 0;
+    if (readtime) {
+        // the read-time ring has one scale per head: every full, occupied tile qualifies
+        for (int w = 0; w < 4; ++w) ap.uniform[w] = 0;
+        const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
+        for (int t = 0; t < h->T && t < 256; ++t) {
+            const int s0 = t * kTileSlots;
+            if (s0 + kTileSlots > h->C) continue;
+            bool occ = true;
+            for (int s = s0; s < s0 + kTileSlots && occ; ++s) occ = (g[s] >= 0);
+            if (occ) ap.uniform[t >> 6] |= 1ull << (t & 63);
+        }
+    } else {
+        refresh_uniform(h, layer);
+        for (int w = 0; w < 4; ++w) ap.uniform[w] = h->uniform[layer][w];
+    }
     ap.sm_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
     ap.status = h->d_status;
     if (launch_attention(ap, h->D, s) != cudaSuccess) return RC_ERR_CUDA;

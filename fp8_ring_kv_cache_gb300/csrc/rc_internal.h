@@ -95,6 +95,9 @@ struct AttnParams {
     int nmt;               // M tiles in qp / qs (even)
     int n, H, C, T, Cpad;
     int masked;            // 1: some slots are empty, read grp
+    // bit j: every slot of KV tile j is occupied by one write group (so one K
+    // and one V scale per head cover the tile); tiles 0..255
+    uint64_t uniform[4];
     float sm_log2;         // log2(e) / sqrt(D)
     int* status;           // device status word
 };
