@@ -29,6 +29,8 @@
 //         the converted V tile from shared memory (B operand).
 // Two M tiles ping-pong so the tensor pipe works on one tile while the other
 // is in softmax.  Output: out = O / sum(P''), fp32.
+#include <type_traits>
+
 #include "rc_device.cuh"
 #include "rc_internal.h"
 
@@ -73,8 +75,8 @@ struct AttnLayout {
     static constexpr uint32_t kV16 = kStage0 + kStages * kStageBytes;  // 2 x [2 halves][D][128 B] fp16
     static constexpr uint32_t kV16One = 2 * D * 128;
     static constexpr uint32_t kV16Bytes = 2 * kV16One;
-    static constexpr uint32_t kSq = kV16 + kV16Bytes;  // fp32 [256] row scales, then svmax (16 B)
-    static constexpr uint32_t kBar = kSq + 2 * kMTile * 4 + 16;
+    static constexpr uint32_t kSq = kV16 + kV16Bytes;  // fp32 [256] row scales
+    static constexpr uint32_t kBar = kSq + 2 * kMTile * 4;
     static constexpr uint32_t kMisc = kBar + 8 * B_COUNT;
     static constexpr uint32_t kTotal = kMisc + 64;
     static constexpr uint32_t kAlloc = kTotal + 1024;  // room to align the base to 1024
@@ -82,91 +84,103 @@ struct AttnLayout {
 
 // ---------------------------------------------------------------- K6 query preparation
 
-constexpr int kPrepWarps = 8;
+// Four threads per query row, each with D/4 consecutive dims, and kPrepHeads
+// heads per block: a thread loads its cos/sin pairs once and keeps them for
+// every head; the row's amax takes two shuffles; accesses are 16 bytes wide.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepRows = kPrepThreads / 4;  // query rows per block
+constexpr int kPrepHeads = 4;                // heads per block
 
 template <int D>
-__global__ void __launch_bounds__(kPrepWarps * 32) q_prep_kernel(QPrepParams p) {
-    constexpr int EPL = D / 32;
-    const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kPrepThreads) q_prep_kernel(QPrepParams p) {
+    constexpr int DPT = D / 4;  // dims per thread (32 or 16)
     const int rows = p.nmt * kMTile;
-    if (static_cast<int>(blockIdx.x) < p.H) {
-        // the head's largest V scale (empty slots hold 0); first in the grid so
-        // these longer blocks start early, eight loads in flight per thread
-        const int h = blockIdx.x;
-        const float* svh = p.sv + static_cast<size_t>(h) * p.Cpad;
-        float m = 0.f;
-#pragma unroll 8
-        for (int i = threadIdx.x; i < p.C; i += kPrepWarps * 32) m = fmaxf(m, svh[i]);
+    const int row = blockIdx.x * kPrepRows + (threadIdx.x >> 2);
+    const int quarter = threadIdx.x & 3;
+    if (row >= rows) return;  // whole groups of four leave together
+    const int dim0 = quarter * DPT;
+    const bool live = row < p.n;
+    float4 cs[DPT / 4];  // (cos, sin) of two pairs each
+    if (live) {
+        const float4* rsrc = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(row) * (D / 2) + dim0 / 2);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        __shared__ float red[kPrepWarps];
-        if (lane == 0) red[threadIdx.x >> 5] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float mm = 0.f;
-            for (int w = 0; w < kPrepWarps; ++w) mm = fmaxf(mm, red[w]);
-            p.svm[h * 4] = mm;
-        }
-        return;
+        for (int i = 0; i < DPT / 4; ++i) cs[i] = __ldg(rsrc + i);
     }
-    const int w = (blockIdx.x - p.H) * kPrepWarps + (threadIdx.x >> 5);
-    if (w >= p.H * rows) return;
-    const int h = w / rows, row = w - h * rows;
-    const int dim0 = lane * EPL;
-    float x[EPL];
-    float amax = 0.f;
-    if (row < p.n) {
-        __nv_bfloat16 qb[EPL];
-        const size_t src = (static_cast<size_t>(row) * p.H + h) * D + dim0;
-        if constexpr (EPL == 4)
-            *reinterpret_cast<uint2*>(qb) = *reinterpret_cast<const uint2*>(p.q + src);
-        else
-            *reinterpret_cast<uint32_t*>(qb) = *reinterpret_cast<const uint32_t*>(p.q + src);
+    const int mt = row / kMTile, rrow = row - mt * kMTile;
+    const int h0 = blockIdx.y * kPrepHeads;
+    // every head's query row in flight at once
+    uint4 qv[kPrepHeads][DPT / 8];
+    if (live) {
 #pragma unroll
-        for (int j = 0; j < EPL / 2; ++j) {
-            const float2 cs = p.rope[static_cast<size_t>(row) * (D / 2) + dim0 / 2 + j];
-            rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), cs.x, cs.y, x[2 * j],
-                        x[2 * j + 1]);
+        for (int k = 0; k < kPrepHeads; ++k) {
+            const int h = min(h0 + k, p.H - 1);
+            const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(row) * p.H + h) * D + dim0);
+#pragma unroll
+            for (int i = 0; i < DPT / 8; ++i) qv[k][i] = __ldg(qsrc + i);
         }
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
-    } else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) x[e] = 0.f;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sq = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
-    const float inv = __frcp_rn(sq);
-    float r[EPL];
+    for (int k = 0; k < kPrepHeads; ++k) {
+        const int h = h0 + k;
+        if (h >= p.H) break;
+        float x[DPT];
+        float amax = 0.f;
+        if (live) {
+            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(qv[k]);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) r[e] = x[e] * inv;
-    const int mt = row / kMTile, rr = row - mt * kMTile;
+            for (int j = 0; j < DPT / 2; ++j) {
+                const float c = (j & 1) ? cs[j >> 1].z : cs[j >> 1].x;
+                const float sn = (j & 1) ? cs[j >> 1].w : cs[j >> 1].y;
+                rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), c, sn, x[2 * j],
+                            x[2 * j + 1]);
+            }
 #pragma unroll
-    for (int pc = 0; pc < kQPieces; ++pc) {
-        uint32_t word = 0;
+            for (int e = 0; e < DPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        } else {
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-            const uint32_t two = e4m3x2(r[e], r[e + 1]);
-            const float2 back = e4m3x2_to_float2(static_cast<uint16_t>(two));
-            r[e] -= back.x;
-            r[e + 1] -= back.y;
-            word |= two << (8 * e);
+            for (int e = 0; e < DPT; ++e) x[e] = 0.f;
         }
-        uint8_t* dst = p.qp + ((static_cast<size_t>(h) * p.nmt + mt) * kQPieces + pc) * (kMTile * D);
-        if constexpr (EPL == 4)
-            *reinterpret_cast<uint32_t*>(dst + ktile_off(rr, dim0, D)) = word;
-        else
-            *reinterpret_cast<uint16_t*>(dst + ktile_off(rr, dim0, D)) = static_cast<uint16_t>(word);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // any scale and inverse serve: the pieces represent x * inv exactly (up
+        // to the third piece's rounding) and the attention kernel multiplies by sq
+        const float sq = (amax > 0.f) ? amax * (1.f / 448.f) : 1.f;
+        const float inv = __fdividef(1.f, sq);
+#pragma unroll
+        for (int e = 0; e < DPT; ++e) x[e] *= inv;
+        uint8_t* dst = p.qp + (static_cast<size_t>(h) * p.nmt + mt) * kQPieces * (kMTile * D);
+#pragma unroll
+        for (int pc = 0; pc < kQPieces; ++pc) {
+            uint32_t w[DPT / 4];
+#pragma unroll
+            for (int k = 0; k < DPT / 4; ++k) {
+                const uint32_t lo = e4m3x2(x[4 * k], x[4 * k + 1]);
+                const uint32_t hi = e4m3x2(x[4 * k + 2], x[4 * k + 3]);
+                if (pc + 1 < kQPieces) {
+                    const float2 bl = e4m3x2_to_float2(static_cast<uint16_t>(lo));
+                    const float2 bh = e4m3x2_to_float2(static_cast<uint16_t>(hi));
+                    x[4 * k] -= bl.x;
+                    x[4 * k + 1] -= bl.y;
+                    x[4 * k + 2] -= bh.x;
+                    x[4 * k + 3] -= bh.y;
+                }
+                w[k] = lo | (hi << 16);
+            }
+            uint8_t* tile = dst + pc * (kMTile * D);
+#pragma unroll
+            for (int c = 0; c < DPT / 16; ++c)
+                *reinterpret_cast<uint4*>(tile + ktile_off(rrow, dim0 + 16 * c, D)) =
+                    make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        if (quarter == 0) p.qs[static_cast<size_t>(h) * rows + row] = sq;
     }
-    if (lane == 0) p.qs[static_cast<size_t>(h) * rows + row] = sq;
 }
 
 template <int D>
 static cudaError_t launch_q_prep_d(const QPrepParams& p, cudaStream_t s) {
     const int rows = p.nmt * kMTile;
-    const int nrb = (p.H * rows + kPrepWarps - 1) / kPrepWarps;
-    q_prep_kernel<D><<<nrb + p.H, kPrepWarps * 32, 0, s>>>(p);
+    dim3 grid((rows + kPrepRows - 1) / kPrepRows, (p.H + kPrepHeads - 1) / kPrepHeads);
+    q_prep_kernel<D><<<grid, kPrepThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -200,7 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);  // [0] tmem, [2] abort
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);  // [0] tmem, [2] abort, [4..11] V-scale maxima
     const float* s_sq = reinterpret_cast<const float*>(smem + Lay::kSq);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -241,9 +255,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
-            // the prepared query pieces, row scales and the head's largest V scale
+            // the prepared query pieces and their row scales
             uint64_t* qf = &bars[B_Q_FULL];
-            mbar_arrive_expect_tx(qf, kQPieces * 2 * kMTile * D + 2 * kMTile * 4 + 16);
+            mbar_arrive_expect_tx(qf, kQPieces * 2 * kMTile * D + 2 * kMTile * 4);
             const int mt0 = blockIdx.x * 2;
             for (int pc = 0; pc < kQPieces; ++pc)
                 for (int i = 0; i < 2; ++i)
@@ -252,7 +266,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                              kMTile * D, qf);
             bulk_g2s(smem + Lay::kSq, p.qs + static_cast<size_t>(h) * p.nmt * kMTile + mt0 * kMTile, 2 * kMTile * 4,
                      qf);
-            bulk_g2s(smem + Lay::kSq + 2 * kMTile * 4, p.svm + h * 4, 16, qf);
             const uint32_t bytes = Lay::kTile + 1024 + (p.masked ? 512 : 0);
             for (int j = 0; j < T; ++j) {
                 const int s = j % kStages;
@@ -359,9 +372,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + 128u * mt;
         const uint32_t o_tm = tmem + lane_off + 256u + static_cast<uint32_t>(D) * mt;
+        // the head's largest V scale (empty slots hold 0): the eight softmax warps
+        // scan the scales while the first scores are computed
+        {
+            const float* svh = p.sv + static_cast<size_t>(h) * p.Cpad;
+            float m = 0.f;
+#pragma unroll 8
+            for (int i = tid - kWarpSm0 * 32; i < p.C; i += 256) m = fmaxf(m, svh[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) reinterpret_cast<float*>(misc)[4 + warp - kWarpSm0] = m;
+            named_barrier_sync(1, 256);
+        }
+        float svmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) svmax = fmaxf(svmax, reinterpret_cast<const float*>(misc)[4 + w]);
         bool ok = warp_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutSoftmax);
         const float a = ok ? s_sq[mt * kMTile + r] * p.sm_log2 : 0.f;  // > 0
-        const float svmax = ok ? s_sq[2 * kMTile] : 1.f;
         const float lsv = (svmax > 0.f) ? lg2_approx(svmax) : 0.f;
         const float2 a2 = make_float2(a, a);
         float m_run = -INFINITY, l_run = 0.f;
@@ -375,118 +402,134 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             const float* ssv = ssk + kTileSlots;
             const int32_t* sgrp = reinterpret_cast<const int32_t*>(ssv + kTileSlots);
             const int nvalid = min(kTileSlots, p.C - j * kTileSlots);
-            const bool full = (nvalid == kTileSlots) && !p.masked;
             // one write group fills the tile: one K and one V scale, no per-column loads
             const bool uni = (p.uniform[j >> 6] >> (j & 63)) & 1ull;
             const float cu = uni ? ssk[0] * a : 0.f;
             const float lsv0 = uni ? lg2_approx(ssv[0]) : 0.f;
             const float isv0 = uni ? ex2(-lsv0) : 1.f;
-            auto valid = [&](int col) { return col < nvalid && (!p.masked || sgrp[col] >= 0); };
             ok = warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax);
             if (!ok) break;
             tc_fence_after();
 
             float m_new, alpha;
             float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            if (uni) {
-                // Uniform tile: the row's 128 scores come into registers with four
-                // TMEM loads and one wait; pass A (the tile max, one max3 tree) and
-                // pass B (the probabilities) both run from the registers.
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld32_async(s_tm, v0);
-                tmem_ld32_async(s_tm + 32, v1);
-                tmem_ld32_async(s_tm + 64, v2);
-                tmem_ld32_async(s_tm + 96, v3);
-                tmem_wait_ld_dep(v0);
-                reg_fence(v1);
-                reg_fence(v2);
-                reg_fence(v3);
-                auto chunk_max = [](const uint32_t (&v)[32]) {
-                    float t[11];
+            // Uniform tile: the row's 128 scores come into registers with four
+            // TMEM loads and one wait; pass A (the tile max, one max3 tree) and
+            // pass B (the probabilities) both run from the registers.  The ring's
+            // last tile (fewer than 128 slots) takes its own instance, so the
+            // column cut costs the full tiles nothing.
+            auto uniform_tile = [&](auto partial) {
+                    uint32_t v0[32], v1[32], v2[32], v3[32];
+                    tmem_ld32_async(s_tm, v0);
+                    tmem_ld32_async(s_tm + 32, v1);
+                    tmem_ld32_async(s_tm + 64, v2);
+                    tmem_ld32_async(s_tm + 96, v3);
+                    tmem_wait_ld_dep(v0);
+                    reg_fence(v1);
+                    reg_fence(v2);
+                    reg_fence(v3);
+                    if constexpr (decltype(partial)::value) {
+                        // the ring's last tile: columns past its end score -inf
+                        auto cut = [&](uint32_t (&v)[32], int c) {
 #pragma unroll
-                    for (int i = 0; i < 10; ++i)
-                        t[i] = max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
-                                    __uint_as_float(v[3 * i + 2]));
-                    t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-                    const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
-                    const float u2 = max3(t[6], t[7], t[8]), u3 = max3(t[9], t[10], u0);
-                    return max3(u1, u2, u3);
-                };
-                const float mxall = fmaxf(fmaxf(chunk_max(v0), chunk_max(v1)), fmaxf(chunk_max(v2), chunk_max(v3)));
-                const float m_tile = mxall * cu;
-                const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
-                m_new = bump ? fmaxf(m_run, m_tile) : m_run;
-                const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha = bump ? ex2(m_run - m_fin) : 1.f;
-                const float msub = m_fin + lsv;
-                // P' = exp2(S c - m - log2(max sv) + log2(sv)): the V scale rides in the exponent
-                const float2 cu2 = make_float2(cu, cu);
-                const float2 nmu2 = make_float2(lsv0 - msub, lsv0 - msub);
-                // all four chunks are computed before the stores, so the exp2 work
-                // runs back to back
-                auto p_chunk = [&](const uint32_t (&v)[32], uint32_t* pk) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float2 x0 = fma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), cu2, nmu2);
-                        const float2 x1 =
-                            fma2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), cu2, nmu2);
-                        const float2 q0 = make_float2(ex2(x0.x), ex2(x0.y));
-                        const float2 q1 = make_float2(ex2(x1.x), ex2(x1.y));
-                        ls[0] = add2(ls[0], q0);
-                        ls[1] = add2(ls[1], q1);
-                        __half2 h0 = __floats2half2_rn(q0.x, q0.y);
-                        __half2 h1 = __floats2half2_rn(q1.x, q1.y);
-                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
-                        pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                            for (int k = 0; k < 32; ++k)
+                                if (32 * c + k >= nvalid) v[k] = __float_as_uint(-INFINITY);
+                        };
+                        cut(v0, 0);
+                        cut(v1, 1);
+                        cut(v2, 2);
+                        cut(v3, 3);
                     }
-                };
-                uint32_t pa[32], pb[32];
-                p_chunk(v0, pa);
-                p_chunk(v1, pa + 16);
-                p_chunk(v2, pb);
-                p_chunk(v3, pb + 16);
-                // P (128 slots as 64 fp16 pairs) goes to columns 0..63
-                tmem_st32(s_tm, pa);
-                tmem_st32(s_tm + 32, pb);
+                    auto chunk_max = [](const uint32_t (&v)[32]) {
+                        float t[11];
+#pragma unroll
+                        for (int i = 0; i < 10; ++i)
+                            t[i] = max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                                        __uint_as_float(v[3 * i + 2]));
+                        t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+                        const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
+                        const float u2 = max3(t[6], t[7], t[8]), u3 = max3(t[9], t[10], u0);
+                        return max3(u1, u2, u3);
+                    };
+                    const float mxall = fmaxf(fmaxf(chunk_max(v0), chunk_max(v1)), fmaxf(chunk_max(v2), chunk_max(v3)));
+                    const float m_tile = mxall * cu;
+                    const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+                    m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+                    const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+                    alpha = bump ? ex2(m_run - m_fin) : 1.f;
+                    const float msub = m_fin + lsv;
+                    // P' = exp2(S c - m - log2(max sv) + log2(sv)): the V scale rides in the exponent
+                    const float2 cu2 = make_float2(cu, cu);
+                    const float2 nmu2 = make_float2(lsv0 - msub, lsv0 - msub);
+                    // all four chunks are computed before the stores, so the exp2 work
+                    // runs back to back
+                    auto p_chunk = [&](const uint32_t (&v)[32], uint32_t* pk) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4) {
+                            const float2 x0 = fma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), cu2, nmu2);
+                            const float2 x1 =
+                                fma2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), cu2, nmu2);
+                            const float2 q0 = make_float2(ex2(x0.x), ex2(x0.y));
+                            const float2 q1 = make_float2(ex2(x1.x), ex2(x1.y));
+                            ls[0] = add2(ls[0], q0);
+                            ls[1] = add2(ls[1], q1);
+                            __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+                            __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+                            pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
+                            pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                        }
+                    };
+                    uint32_t pa[32], pb[32];
+                    p_chunk(v0, pa);
+                    p_chunk(v1, pa + 16);
+                    p_chunk(v2, pb);
+                    p_chunk(v3, pb + 16);
+                    // P (128 slots as 64 fp16 pairs) goes to columns 0..63
+                    tmem_st32(s_tm, pa);
+                    tmem_st32(s_tm + 32, pb);
+            };
+            if (uni && nvalid == kTileSlots) {
+                uniform_tile(std::false_type{});
+            } else if (uni) {
+                uniform_tile(std::true_type{});
             } else {
                 // Per-column scales (and, on a partial or masked tile, a validity
                 // test): pass A and pass B each read the scores from TMEM in
-                // 32-column chunks, the next chunk loading while one is used.
+                // 32-column chunks.
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // validity of four columns as selects; all of a chunk's scale (and
+                // group) loads are issued together, none sits behind a branch
+                auto ok4 = [&](int col, bool (&ok)[4]) {
+                    const int4 g4 = p.masked ? *reinterpret_cast<const int4*>(sgrp + col) : make_int4(0, 0, 0, 0);
+                    ok[0] = (col < nvalid) && g4.x >= 0;
+                    ok[1] = (col + 1 < nvalid) && g4.y >= 0;
+                    ok[2] = (col + 2 < nvalid) && g4.z >= 0;
+                    ok[3] = (col + 3 < nvalid) && g4.w >= 0;
+                };
                 auto max_chunk = [&](const uint32_t (&v)[32], int c) {
-                    if (full) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
-                            const float2 x0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                                   make_float2(s4.x, s4.y));
-                            const float2 x1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                                   make_float2(s4.z, s4.w));
-                            mx[(k >> 2) & 1] = max3(mx[(k >> 2) & 1], x0.x, x0.y);
-                            mx[2 + ((k >> 2) & 1)] = max3(mx[2 + ((k >> 2) & 1)], x1.x, x1.y);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int col = 32 * c + k;
-                            if (valid(col)) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]) * ssk[col]);
-                        }
+                    for (int k = 0; k < 32; k += 4) {
+                        const int col = 32 * c + k;
+                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
+                        bool ok[4];
+                        ok4(col, ok);
+                        const float2 y0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                               make_float2(s4.x, s4.y));
+                        const float2 y1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                               make_float2(s4.z, s4.w));
+                        mx[(k >> 2) & 1] =
+                            max3(mx[(k >> 2) & 1], ok[0] ? y0.x : -INFINITY, ok[1] ? y0.y : -INFINITY);
+                        mx[2 + ((k >> 2) & 1)] =
+                            max3(mx[2 + ((k >> 2) & 1)], ok[2] ? y1.x : -INFINITY, ok[3] ? y1.y : -INFINITY);
                     }
                 };
-                {
-                    uint32_t va[32], vb[32];
-                    tmem_ld32_async(s_tm, va);
-                    tmem_wait_ld_dep(va);
-                    tmem_ld32_async(s_tm + 32, vb);
-                    max_chunk(va, 0);
-                    tmem_wait_ld_dep(vb);
-                    tmem_ld32_async(s_tm + 64, va);
-                    max_chunk(vb, 1);
-                    tmem_wait_ld_dep(va);
-                    tmem_ld32_async(s_tm + 96, vb);
-                    max_chunk(va, 2);
-                    tmem_wait_ld_dep(vb);
-                    max_chunk(vb, 3);
+                // rare (partial, masked or mixed-group tiles): a compact loop, one
+                // chunk at a time
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(s_tm + 32 * c, v);
+                    max_chunk(v, c);
                 }
                 const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
                 const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
@@ -497,57 +540,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 const float2 nm2 = make_float2(-msub, -msub);
                 auto p_chunk = [&](const uint32_t (&v)[32], int c) {
                     uint32_t pk[16];
-                    if (full) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 s4 = *reinterpret_cast<const float4*>(ssk + 32 * c + k);
-                            const float4 v4 = *reinterpret_cast<const float4*>(ssv + 32 * c + k);
-                            const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                                        make_float2(s4.x, s4.y)), a2, nm2);
-                            const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                                        make_float2(s4.z, s4.w)), a2, nm2);
-                            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-                            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-                            ls[0] = add2(ls[0], p0);
-                            ls[1] = add2(ls[1], p1);
-                            const float2 q0 = mul2(p0, make_float2(v4.x, v4.y));
-                            const float2 q1 = mul2(p1, make_float2(v4.z, v4.w));
-                            __half2 h0 = __floats2half2_rn(q0.x, q0.y);
-                            __half2 h1 = __floats2half2_rn(q1.x, q1.y);
-                            pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
-                            pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
-                            const int c0 = 32 * c + k, c1 = c0 + 1;
-                            const float p0 = valid(c0) ? ex2(__fmaf_rn(__uint_as_float(v[k]) * ssk[c0], a, -msub)) : 0.f;
-                            const float p1 =
-                                valid(c1) ? ex2(__fmaf_rn(__uint_as_float(v[k + 1]) * ssk[c1], a, -msub)) : 0.f;
-                            ls[0].x += p0;
-                            ls[1].y += p1;
-                            __half2 hp = __floats2half2_rn(p0 * (valid(c0) ? ssv[c0] : 0.f),
-                                                           p1 * (valid(c1) ? ssv[c1] : 0.f));
-                            pk[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
-                        }
+                    for (int k = 0; k < 32; k += 4) {
+                        const int col = 32 * c + k;
+                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
+                        const float4 v4 = *reinterpret_cast<const float4*>(ssv + col);
+                        bool ok[4];
+                        ok4(col, ok);
+                        const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                                    make_float2(s4.x, s4.y)), a2, nm2);
+                        const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                                    make_float2(s4.z, s4.w)), a2, nm2);
+                        const float2 p0 = make_float2(ok[0] ? ex2(x0.x) : 0.f, ok[1] ? ex2(x0.y) : 0.f);
+                        const float2 p1 = make_float2(ok[2] ? ex2(x1.x) : 0.f, ok[3] ? ex2(x1.y) : 0.f);
+                        ls[0] = add2(ls[0], p0);
+                        ls[1] = add2(ls[1], p1);
+                        const float2 q0 =
+                            make_float2(ok[0] ? p0.x * v4.x : 0.f, ok[1] ? p0.y * v4.y : 0.f);
+                        const float2 q1 =
+                            make_float2(ok[2] ? p1.x * v4.z : 0.f, ok[3] ? p1.y * v4.w : 0.f);
+                        __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+                        __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
+                        pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
                     }
                     // P chunk c goes to columns 16c..16c+15, which were read in chunks <= c
                     tmem_st16(s_tm + 16 * c, pk);
                 };
-                {
-                    uint32_t va[32], vb[32];
-                    tmem_ld32_async(s_tm, va);
-                    tmem_wait_ld_dep(va);
-                    tmem_ld32_async(s_tm + 32, vb);
-                    p_chunk(va, 0);
-                    tmem_wait_ld_dep(vb);
-                    tmem_ld32_async(s_tm + 64, va);
-                    p_chunk(vb, 1);
-                    tmem_wait_ld_dep(va);
-                    tmem_ld32_async(s_tm + 96, vb);
-                    p_chunk(va, 2);
-                    tmem_wait_ld_dep(vb);
-                    p_chunk(vb, 3);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(s_tm + 32 * c, v);
+                    p_chunk(v, c);
                 }
             }
             tmem_st_wait();

@@ -103,6 +103,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, AbortS
     }
 }
 
+// Barrier `id` (1..15) among `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy (both addresses 16-byte aligned), L1 bypassed.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ bulk copies
 // Global -> shared bulk copy that completes `bytes` on the mbarrier.
 // Both addresses 16-byte aligned, bytes a multiple of 16.

@@ -6,6 +6,7 @@
 // em tempo real com batch size 1": the window advances without copies): token
 // at position p lives in slot floormod(p - delta_total, C).  A delta rotation
 // adds delta to every stored position and to delta_total, so no token moves.
+#include <algorithm>
 #include <array>
 #include <cmath>
 #include <cstdio>
@@ -62,7 +63,6 @@ struct rc_cache {
     float* d_rt_sv = nullptr;
     uint8_t* d_qp = nullptr;   // prepared query pieces of one attention call
     float* d_qs = nullptr;     // their row scales
-    float* d_svm = nullptr;    // per-head largest V scale
     int nmt_max = 0;           // 128-row query tiles for max_write queries (even)
     RopeEntry pool[kPoolEntries];
     uint64_t clock = 0;
@@ -113,7 +113,6 @@ void free_all(rc_cache* h) {
     cudaFree(h->d_rt_sv);
     cudaFree(h->d_qp);
     cudaFree(h->d_qs);
-    cudaFree(h->d_svm);
     for (auto& e : h->pool) {
         cudaFree(e.d_table);
         cudaFree(e.d_pos);
@@ -130,10 +129,11 @@ void refresh_uniform(rc_cache* h, int layer) {
     m = {0, 0, 0, 0};
     const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
     for (int t = 0; t < h->T && t < 256; ++t) {
-        const int s0 = t * kTileSlots;
-        if (s0 + kTileSlots > h->C || g[s0] < 0) continue;
+        // the ring's slots of the tile (the last tile may end before 128)
+        const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, h->C);
+        if (g[s0] < 0) continue;
         bool same = true;
-        for (int s = s0 + 1; s < s0 + kTileSlots && same; ++s) same = (g[s] == g[s0]);
+        for (int s = s0 + 1; s < s1 && same; ++s) same = (g[s] == g[s0]);
         if (same) m[t >> 6] |= 1ull << (t & 63);
     }
     h->uniform_dirty[layer] = 0;
@@ -279,7 +279,6 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     h->nmt_max = 2 * ((h->max_write + 255) / 256);
     st |= dmalloc(&h->d_qp, static_cast<size_t>(h->H) * h->nmt_max * 3 * 128 * h->D);
     st |= dmalloc(&h->d_qs, static_cast<size_t>(h->H) * h->nmt_max * 128);
-    st |= dmalloc(&h->d_svm, static_cast<size_t>(h->H) * 4);
     for (auto& e : h->pool) {
         st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
         st |= dmalloc(&e.d_pos, static_cast<size_t>(h->max_write));
@@ -520,24 +519,19 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     }
     ap.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
     // query preparation: rotated, scaled, split into E4M3 pieces in the
-    // attention kernel's shared-memory layout; and each head's largest V scale
+    // attention kernel's shared-memory layout
     QPrepParams qp{};
     qp.q = static_cast<const __nv_bfloat16*>(Q_bf16);
     qp.rope = h->pool[entry].d_table;
-    qp.sv = ap.sv;
     qp.qp = h->d_qp;
     qp.qs = h->d_qs;
-    qp.svm = h->d_svm;
     qp.n = n;
     qp.H = h->H;
-    qp.C = h->C;
-    qp.Cpad = h->Cpad;
     qp.nmt = 2 * ((n + 255) / 256);
     if (launch_q_prep(qp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
     ap.qp = h->d_qp;
     ap.qs = h->d_qs;
-    ap.svm = h->d_svm;
     ap.nmt = qp.nmt;
     ap.q = static_cast<const __nv_bfloat16*>(Q_bf16);
     ap.rope = h->pool[entry].d_table;
@@ -549,14 +543,13 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     ap.Cpad = h->Cpad;
     ap.masked = (h->occupancy[layer] < h->C) ? 1 : 0;
     if (readtime) {
-        // the read-time ring has one scale per head: every full, occupied tile qualifies
+        // the read-time ring has one scale per head: every fully occupied tile qualifies
         for (int w = 0; w < 4; ++w) ap.uniform[w] = 0;
         const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
         for (int t = 0; t < h->T && t < 256; ++t) {
-            const int s0 = t * kTileSlots;
-            if (s0 + kTileSlots > h->C) continue;
+            const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, h->C);
             bool occ = true;
-            for (int s = s0; s < s0 + kTileSlots && occ; ++s) occ = (g[s] >= 0);
+            for (int s = s0; s < s1 && occ; ++s) occ = (g[s] >= 0);
             if (occ) ap.uniform[t >> 6] |= 1ull << (t & 63);
         }
     } else {

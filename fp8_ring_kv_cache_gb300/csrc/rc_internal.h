@@ -72,11 +72,9 @@ struct ReadtimeParams {
 struct QPrepParams {
     const __nv_bfloat16* q;  // [n][H][D]
     const float2* rope;      // [n][D/2]
-    const float* sv;         // layer [H][Cpad]
     uint8_t* qp;             // [H][nmt][3][128][D] (rows >= n are zero)
     float* qs;               // [H][nmt * 128] row scales (1 for rows >= n)
-    float* svm;              // [H][4] largest V scale (element 0)
-    int n, H, C, Cpad, nmt;  // nmt: 128-row M tiles, rounded up to even
+    int n, H, nmt;           // nmt: 128-row M tiles, rounded up to even
 };
 
 // K4: FP8 attention over one layer's ring.
@@ -91,12 +89,12 @@ struct AttnParams {
     float* out;            // [n][H][D]
     const uint8_t* qp;     // prepared query pieces (QPrepParams::qp)
     const float* qs;       // row scales
-    const float* svm;      // per-head largest V scale
     int nmt;               // M tiles in qp / qs (even)
     int n, H, C, T, Cpad;
     int masked;            // 1: some slots are empty, read grp
-    // bit j: every slot of KV tile j is occupied by one write group (so one K
-    // and one V scale per head cover the tile); tiles 0..255
+    // bit j: every ring slot of KV tile j (the last tile may hold fewer than
+    // 128) is occupied by one write group, so one K and one V scale per head
+    // cover the tile; tiles 0..255
     uint64_t uniform[4];
     float sm_log2;         // log2(e) / sqrt(D)
     int* status;           // device status word

@@ -5,12 +5,13 @@
 // K1 rope_table_kernel: cos/sin of p * theta_i for the n positions of a write,
 //    angle formed in fp64 so large positions keep full accuracy.
 // K2 write_kernel: one thread-block cluster of 8 CTAs per head.  Each CTA
-//    bulk-copies its share of the n tokens (one 256-byte bf16 K row and V row
-//    per token) into shared memory, rotates K, and reduces the head's amax for
+//    copies its share of the n tokens (one bf16 K row and V row per token)
+//    into shared memory, rotates K, and reduces the head's amax for
 //    K and for V across the cluster through distributed shared memory; then
 //    every element becomes the E4M3 code of fl32(x / s) with
 //    s = fl32(amax / 448) and is scattered into its ring slot: K rows into the
 //    swizzled K tile, V through a shared-memory transpose into the Vt tile.
+//    Rows are staged with 16-byte cp.async copies.
 //    HBM traffic is one read of K and V and one write of the codes.
 #include "rc_device.cuh"
 #include "rc_internal.h"
@@ -39,20 +40,20 @@ constexpr int kWriteCluster = 8;
 constexpr int kWriteWarps = 8;
 constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kWriteTB = 96;  // tokens staged in shared memory per batch
+constexpr int kWritePer = kWriteTB / kWriteWarps;  // tokens a warp takes per batch
 
 template <int D>
 struct WriteSmem {
-    static constexpr int kVRow = D + 4;  // padded V staging row (consecutive tokens hit different banks)
+    static constexpr int kVRow = D + 16;  // V staging row: 16-byte aligned, 16-byte reads of consecutive rows spread over the banks
     static constexpr uint32_t kK = 0;                                   // bf16 [TB][D]
     static constexpr uint32_t kV = kK + kWriteTB * D * 2;               // bf16 [TB][D]
     static constexpr uint32_t kStage = kV + kWriteTB * D * 2;           // u8 [TB][kVRow]
     static constexpr uint32_t kSlot = kStage + kWriteTB * kVRow;        // int32 [TB]
-    static constexpr uint32_t kBar = (kSlot + kWriteTB * 4 + 7) / 8 * 8;
-    static constexpr uint32_t kTotal = kBar + 16;
+    static constexpr uint32_t kTotal = kSlot + kWriteTB * 4;
 };
 
 template <int D>
-__global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteThreads)
+__global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteThreads, 3)
     write_kernel(WriteParams p) {
     using S = WriteSmem<D>;
     constexpr int EPL = D / 32;       // elements per lane (4 or 2)
@@ -63,11 +64,9 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     __nv_bfloat16* vbuf = reinterpret_cast<__nv_bfloat16*>(smem + S::kV);
     uint8_t* vstage = smem + S::kStage;
     int32_t* sslot = reinterpret_cast<int32_t*>(smem + S::kSlot);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kBar);
     __shared__ float red[2][kWriteWarps];
     __shared__ float cta_amax[2];
     __shared__ float scales[2];
-    __shared__ uint32_t abort_flag;
 
     const int h = blockIdx.y;
     const int crank = blockIdx.x;     // the cluster spans blockIdx.x
@@ -77,14 +76,6 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     const int t1 = min(p.n, t0 + tpc);
     const int nbatch = (t1 - t0 + kWriteTB - 1) / kWriteTB;
     const int dim0 = lane * EPL;
-    AbortState ab{&abort_flag, p.status};
-
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
 
     // slot of token t: floormod(pos - delta_total, C); an arithmetic run starts at slot0
     auto slot_of = [&](int t) -> int {
@@ -94,25 +85,35 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         }
         return static_cast<int>(floormod64(p.pos[t] - p.delta_total, p.C));
     };
-    // bring tokens [tb, tb + cnt) of this head into shared memory: two bulk
-    // copies (K row, V row) per token, all in flight on one mbarrier phase
-    uint32_t phase = 0;
-    auto stage_batch = [&](int tb, int cnt) -> bool {
-        if (warp == 0) {
-            if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 2 * ROWB);
-            __syncwarp();
-            for (int tl = lane; tl < cnt; tl += 32) {
-                const size_t src = (static_cast<size_t>(tb + tl) * p.H + h) * D;
-                bulk_g2s(kbuf + tl * D, p.K + src, ROWB, bar);
-                bulk_g2s(vbuf + tl * D, p.V + src, ROWB, bar);
-            }
+    // bring tokens [tb, tb + cnt) of this head into shared memory: every thread
+    // copies 16-byte pieces of the K and V rows with cp.async (many small
+    // row-sized bulk copies were several times slower)
+    auto stage_batch = [&](int tb, int cnt) {
+        constexpr int kUnits = ROWB / 16;  // 16-byte pieces of one row
+        const int total = cnt * 2 * kUnits;
+        for (int u = threadIdx.x; u < total; u += kWriteThreads) {
+            const int tl = u / (2 * kUnits), r = u - tl * (2 * kUnits);
+            const int which = r / kUnits, c = r - which * kUnits;
+            const __nv_bfloat16* src = (which ? p.V : p.K) + (static_cast<size_t>(tb + tl) * p.H + h) * D + c * 8;
+            __nv_bfloat16* dst = (which ? vbuf : kbuf) + tl * D + c * 8;
+            cp_async16(dst, src);
         }
-        const bool ok = mbar_wait(bar, phase & 1, ab, kDevTimeoutLoader);
-        ++phase;
-        return ok;
+        cp_async_wait_all();
+        __syncthreads();
+    };
+    // cos/sin pairs of this lane's dims for the warp's tokens of a batch, all
+    // loads in flight at once (one L2 round trip instead of one per token)
+    auto fetch_rope = [&](int tb, int cnt, float2 (&cs)[kWritePer][EPL / 2]) {
+#pragma unroll
+        for (int i = 0; i < kWritePer; ++i) {
+            const int tl = warp + kWriteWarps * i;
+            const float2* rr = p.rope + static_cast<size_t>(tb + min(tl, cnt - 1)) * HALF + dim0 / 2;
+#pragma unroll
+            for (int j = 0; j < EPL / 2; ++j) cs[i][j] = __ldg(rr + j);
+        }
     };
     // token tl of the staged batch: K rotated at its position (EPL values of this lane) and V
-    auto row = [&](int tb, int tl, float (&k)[EPL], float (&v)[EPL]) {
+    auto row = [&](int tl, const float2 (&cs)[EPL / 2], float (&k)[EPL], float (&v)[EPL]) {
         __nv_bfloat16 kb[EPL], vb[EPL];
         if constexpr (EPL == 4) {
             *reinterpret_cast<uint2*>(kb) = *reinterpret_cast<const uint2*>(kbuf + tl * D + dim0);
@@ -121,28 +122,29 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
             *reinterpret_cast<uint32_t*>(kb) = *reinterpret_cast<const uint32_t*>(kbuf + tl * D + dim0);
             *reinterpret_cast<uint32_t*>(vb) = *reinterpret_cast<const uint32_t*>(vbuf + tl * D + dim0);
         }
-        const float2* rr = p.rope + static_cast<size_t>(tb + tl) * HALF + dim0 / 2;
 #pragma unroll
-        for (int j = 0; j < EPL / 2; ++j) {
-            const float2 cs = rr[j];
-            rotate_pair(__bfloat162float(kb[2 * j]), __bfloat162float(kb[2 * j + 1]), cs.x, cs.y, k[2 * j],
+        for (int j = 0; j < EPL / 2; ++j)
+            rotate_pair(__bfloat162float(kb[2 * j]), __bfloat162float(kb[2 * j + 1]), cs[j].x, cs[j].y, k[2 * j],
                         k[2 * j + 1]);
-        }
 #pragma unroll
         for (int e = 0; e < EPL; ++e) v[e] = __bfloat162float(vb[e]);
     };
 
     // ---- phase 1: per-head amax of rotated K and of V over this CTA's tokens
     float amk = 0.f, amv = 0.f;
-    bool ok = true;
     for (int b = 0; b < nbatch; ++b) {
         const int tb = t0 + b * kWriteTB;
         const int cnt = min(kWriteTB, t1 - tb);
-        ok = stage_batch(tb, cnt) && ok;
-        if (ok) {
-            for (int tl = warp; tl < cnt; tl += kWriteWarps) {
+        float2 cs[kWritePer][EPL / 2];
+        fetch_rope(tb, cnt, cs);
+        stage_batch(tb, cnt);
+        {
+#pragma unroll
+            for (int i = 0; i < kWritePer; ++i) {
+                const int tl = warp + kWriteWarps * i;
+                if (tl >= cnt) break;
                 float k[EPL], v[EPL];
-                row(tb, tl, k, v);
+                row(tl, cs[i], k, v);
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
                     amk = fmaxf(amk, fabsf(k[e]));
@@ -196,16 +198,18 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     const float rK = __frcp_rn(sK), rV = __frcp_rn(sV);
 
     // ---- phase 2: quantise and scatter (a single batch is still staged)
-    for (int b = 0; b < nbatch && ok; ++b) {
+    for (int b = 0; b < nbatch; ++b) {
         const int tb = t0 + b * kWriteTB;
         const int cnt = min(kWriteTB, t1 - tb);
-        if (nbatch > 1) {
-            ok = stage_batch(tb, cnt);
-            if (!ok) break;
-        }
-        for (int tl = warp; tl < cnt; tl += kWriteWarps) {
+        float2 cs[kWritePer][EPL / 2];
+        fetch_rope(tb, cnt, cs);
+        if (nbatch > 1) stage_batch(tb, cnt);
+#pragma unroll
+        for (int i = 0; i < kWritePer; ++i) {
+            const int tl = warp + kWriteWarps * i;
+            if (tl >= cnt) break;
             float k[EPL], v[EPL];
-            row(tb, tl, k, v);
+            row(tl, cs[i], k, v);
             const int slot = slot_of(tb + tl);
             if (lane == 0) sslot[tl] = slot;
             uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
@@ -233,13 +237,21 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
             }
         }
         __syncthreads();
-        // V transposed: a warp takes one dim row, its lanes consecutive tokens
+        // V transposed: warp w takes dims [16w', 16w' + 16) (w' = w, w + 8, ...),
+        // each lane its tokens; one 16-byte shared load gives a token's 16
+        // codes, which go to 16 rows of the token's Vt column
         uint8_t* vhead = p.vt + static_cast<size_t>(h) * p.T * (D * kTileSlots);
-        for (int d = warp; d < D; d += kWriteWarps) {
-            for (int tl = lane; tl < cnt; tl += 32) {
-                const int slot = sslot[tl];
-                vhead[static_cast<size_t>(slot >> 7) * (D * kTileSlots) + vtile_off(d, slot & 127)] =
-                    vstage[tl * S::kVRow + d];
+        for (int tl = lane; tl < cnt; tl += 32) {
+            const int slot = sslot[tl];
+            // Vt byte of (d, slot): tile base + d * 128 + ((chunk ^ (d & 7)) << 4) + (slot & 15)
+            uint8_t* base = vhead + static_cast<size_t>(slot >> 7) * (D * kTileSlots) + (slot & 15);
+            const int chunk = (slot >> 4) & 7;
+            for (int d0 = warp * 16; d0 < D; d0 += kWriteWarps * 16) {
+                const uint4 w = *reinterpret_cast<const uint4*>(vstage + tl * S::kVRow + d0);
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    base[(d0 + k) * 128 + ((chunk ^ (k & 7)) << 4)] = static_cast<uint8_t>(words[k >> 2] >> (8 * (k & 3)));
             }
         }
         __syncthreads();
