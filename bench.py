@@ -42,7 +42,11 @@ READTIME_EXTRA_BYTES = C * H * D * (2 + 2) + C * H * D * 2  # bf16 store read + 
 # dram bytes per launch measured by ncu (profiles/), valid only for the kernel
 # source they were taken on
 TRAFFIC = {
-    "attention": {"bytes": None, "src_sha256": None},
+    # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
+    # the production call (ncu, profiles/attn_kernel_production_call.md), valid
+    # while rc_attention.cu has this hash
+    "attention": {"bytes": 92.70e6,
+                  "src_sha256": "98043bc625d0c459ba2cf08e96058fdf2679447a146448934536327344d1cfa5"},
 }
 
 
