@@ -104,6 +104,24 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(values: list[float], device, world: int) -> list[float]:
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor(values, device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world: int, steps: int, elapsed_ms: float) -> float:
+    """Calls per second of the whole job: every rank runs `steps` chunks of
+    CALLS_PER_CHUNK calls on its own GPU; the job takes the slowest rank's time."""
+    return world * CALLS_PER_CHUNK * steps / (elapsed_ms / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
@@ -209,12 +227,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     e2e = run_e2e(args, dev, K, V, Q, mult, kp, vp)
 
     # ---- max over ranks
-    if world > 1:
-        t = torch.tensor([elapsed_ms, e2e["elapsed_ms"]], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = e2e["elapsed_ms"]
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["elapsed_ms"]], dev, world)
     if rank != 0:
         return None
 
@@ -222,7 +235,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]           # fp8 dense = 2x bf16 dense (nominal ratio)
     hbm = peaks["hbm_gbs"]
     ms_step = elapsed_ms / args.steps
-    value = world * CALLS_PER_CHUNK * args.steps / (elapsed_ms / 1e3)
+    value = job_throughput(world, args.steps, elapsed_ms)
     att_us = statistics.mean(a_times)
     achieved_tflops = ATTN_FLOP / (att_us * 1e-6) / 1e12
     w_us = statistics.mean(w_times)
@@ -271,7 +284,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "readtime_ablation": ab,
             "hbm_peak_gbs": hbm, "peak_source": peak_src,
         },
-        "e2e": {"value": round(world * CALLS_PER_CHUNK * args.steps / (e2e_ms / 1e3), 2), "unit": "calls/s",
+        "e2e": {"value": round(job_throughput(world, args.steps, e2e_ms), 2), "unit": "calls/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms / args.steps, 3)},
         "gpu_launches": int(launches),
