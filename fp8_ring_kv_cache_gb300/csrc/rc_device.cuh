@@ -108,6 +108,16 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// 16-byte read-only global load that does not allocate in L1 (the data is
+// used once; allocating would evict lines the SM's shared memory traffic needs).
+__device__ __forceinline__ uint4 ldg_nc_na_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ------------------------------------------------------------------ cp.async
 // 16-byte global -> shared copy (both addresses 16-byte aligned), L1 bypassed.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
