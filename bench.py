@@ -341,7 +341,9 @@ def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
 def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
     """The same chunk through the public API with pinned host inputs: every call
     copies its K, V, Q host->device and its output device->host, inside the
-    timed region, on a copy stream overlapped with the compute stream."""
+    timed region.  Inputs go up on one copy stream and outputs come down on
+    another (the two directions run at once), each three buffers deep, so the
+    copies of neighbouring calls overlap the compute stream."""
     import numpy as np
     import torch
 
@@ -350,47 +352,52 @@ def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
     cache = rc.RingKVCache(L, H, D, C, max_write=C)
     for layer in range(L):
         cache.write(layer, kp, vp, np.arange(0, PREFILL))
-    nbuf = 8
+    nbuf, nb = 8, 3
     hk = [K[0, i].cpu().pin_memory() for i in range(nbuf)]
     hv = [V[0, i].cpu().pin_memory() for i in range(nbuf)]
     hq = [Q[0, i].cpu().pin_memory() for i in range(nbuf)]
-    hout = [torch.empty(N_NEW, H, D, dtype=torch.float32).pin_memory() for _ in range(2)]
-    dk = [torch.empty_like(K[0, 0]) for _ in range(2)]
-    dv = [torch.empty_like(K[0, 0]) for _ in range(2)]
-    dq = [torch.empty_like(K[0, 0]) for _ in range(2)]
-    dout = [torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev) for _ in range(2)]
+    hout = [torch.empty(N_NEW, H, D, dtype=torch.float32).pin_memory() for _ in range(nb)]
+    dk = [torch.empty_like(K[0, 0]) for _ in range(nb)]
+    dv = [torch.empty_like(K[0, 0]) for _ in range(nb)]
+    dq = [torch.empty_like(K[0, 0]) for _ in range(nb)]
+    dout = [torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev) for _ in range(nb)]
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     pos = np.arange(PREFILL, PREFILL + N_NEW)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
-    out_ready = [torch.cuda.Event() for _ in range(2)]
-    drained = [torch.cuda.Event() for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(nb)]
+    consumed = [torch.cuda.Event() for _ in range(nb)]
+    out_ready = [torch.cuda.Event() for _ in range(nb)]
+    drained = [torch.cuda.Event() for _ in range(nb)]
     for e in consumed + drained:
         e.record(comp)
+    calls = [(pas, layer) for pas in range(PASSES) for layer in range(L)]
+
+    def upload(i):
+        b = i % nb
+        with torch.cuda.stream(up):
+            up.wait_event(consumed[b])
+            dk[b].copy_(hk[i % nbuf], non_blocking=True)
+            dv[b].copy_(hv[i % nbuf], non_blocking=True)
+            dq[b].copy_(hq[i % nbuf], non_blocking=True)
+            in_ready[b].record(up)
 
     def chunk():
-        i = 0
-        for pas in range(PASSES):
-            for layer in range(L):
-                b = i & 1
-                with torch.cuda.stream(copy):
-                    copy.wait_event(consumed[b])
-                    dk[b].copy_(hk[i % nbuf], non_blocking=True)
-                    dv[b].copy_(hv[i % nbuf], non_blocking=True)
-                    dq[b].copy_(hq[i % nbuf], non_blocking=True)
-                    in_ready[b].record(copy)
-                comp.wait_event(in_ready[b])
-                comp.wait_event(drained[b])
-                cache.write(layer, dk[b], dv[b], pos)
-                cache.attend(layer, dq[b], dout[b])
-                consumed[b].record(comp)
-                out_ready[b].record(comp)
-                with torch.cuda.stream(copy):
-                    copy.wait_event(out_ready[b])
-                    hout[b].copy_(dout[b], non_blocking=True)
-                    drained[b].record(copy)
-                i += 1
+        upload(0)
+        for i, (pas, layer) in enumerate(calls):
+            b = i % nb
+            if i + 1 < len(calls):
+                upload(i + 1)              # the next call's inputs go up during this call
+            comp.wait_event(in_ready[b])
+            comp.wait_event(drained[b])
+            cache.write(layer, dk[b], dv[b], pos)
+            cache.attend(layer, dq[b], dout[b])
+            consumed[b].record(comp)
+            out_ready[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[b])
+                hout[b].copy_(dout[b], non_blocking=True)
+                drained[b].record(down)
 
     for _ in range(args.warmup):
         chunk()
