@@ -3,16 +3,13 @@
 // cpdf.ai "Blackwell, escalabilidade e limites do decodificador": the FP8
 // attention kernel with per-head scales that the B200 build lacked).
 //
-// K6 q_prep_kernel: one warp per (query row, head): RoPE at the row's position,
-//    one fp32 scale sq = fl32(amax / 448) per row, and three E4M3 pieces
-//    (hi + mid + lo, 12 significant bits) of q / sq, written straight into the
-//    swizzled shared-memory image the attention kernel's A operand needs.
-//    The first H blocks take each head's largest V scale.
 // K4 attn_kernel: one CTA = one head x 256 query rows (two 128-row M tiles),
-//    448 threads:
-//   warp 0        loader: bulk copies of the prepared query pieces, then one
-//                 bulk copy per K tile and scale vectors per 128-slot KV tile,
-//                 double-buffered (mbarrier + complete_tx)
+//    384 threads.  Prologue, all warps: the CTA's queries are rotated, given
+//    one scale sq = amax / 448 per row and split into three E4M3 pieces
+//    (hi + mid + lo, ~12 significant bits) of q / sq, written straight into
+//    the swizzled A-operand image in shared memory.  Then:
+//   warp 0        loader: one bulk copy per K tile and the scale vectors per
+//                 128-slot KV tile, double-buffered (mbarrier + complete_tx)
 //   warp 1        MMA issuer (one lane) and TMEM owner (512 columns)
 //   warps 2..5    softmax group 0 (rows 0..127; one row per thread / TMEM lane)
 //   warps 6..9    softmax group 1 (rows 128..255)
@@ -61,8 +58,7 @@ enum : int {
     B_P_FULL = 12,     // [2]
     B_O_DONE = 14,     // [2]
     B_DRAIN = 16,
-    B_Q_FULL = 17,
-    B_COUNT = 18
+    B_COUNT = 17
 };
 
 template <int D>
@@ -83,110 +79,6 @@ struct AttnLayout {
 };
 
 // ---------------------------------------------------------------- K6 query preparation
-
-// Four threads per query row, each with D/4 consecutive dims, and kPrepHeads
-// heads per block: a thread loads its cos/sin pairs once and keeps them for
-// every head; the row's amax takes two shuffles; accesses are 16 bytes wide.
-constexpr int kPrepThreads = 256;
-constexpr int kPrepRows = kPrepThreads / 4;  // query rows per block
-constexpr int kPrepHeads = 4;                // heads per block
-
-template <int D>
-__global__ void __launch_bounds__(kPrepThreads) q_prep_kernel(QPrepParams p) {
-    constexpr int DPT = D / 4;  // dims per thread (32 or 16)
-    const int rows = p.nmt * kMTile;
-    const int row = blockIdx.x * kPrepRows + (threadIdx.x >> 2);
-    const int quarter = threadIdx.x & 3;
-    if (row >= rows) return;  // whole groups of four leave together
-    const int dim0 = quarter * DPT;
-    const bool live = row < p.n;
-    float4 cs[DPT / 4];  // (cos, sin) of two pairs each
-    if (live) {
-        const float4* rsrc = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(row) * (D / 2) + dim0 / 2);
-#pragma unroll
-        for (int i = 0; i < DPT / 4; ++i) cs[i] = __ldg(rsrc + i);
-    }
-    const int mt = row / kMTile, rrow = row - mt * kMTile;
-    const int h0 = blockIdx.y * kPrepHeads;
-    // every head's query row in flight at once
-    uint4 qv[kPrepHeads][DPT / 8];
-    if (live) {
-#pragma unroll
-        for (int k = 0; k < kPrepHeads; ++k) {
-            const int h = min(h0 + k, p.H - 1);
-            const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(row) * p.H + h) * D + dim0);
-#pragma unroll
-            for (int i = 0; i < DPT / 8; ++i) qv[k][i] = __ldg(qsrc + i);
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < kPrepHeads; ++k) {
-        const int h = h0 + k;
-        if (h >= p.H) break;
-        float x[DPT];
-        float amax = 0.f;
-        if (live) {
-            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(qv[k]);
-#pragma unroll
-            for (int j = 0; j < DPT / 2; ++j) {
-                const float c = (j & 1) ? cs[j >> 1].z : cs[j >> 1].x;
-                const float sn = (j & 1) ? cs[j >> 1].w : cs[j >> 1].y;
-                rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), c, sn, x[2 * j],
-                            x[2 * j + 1]);
-            }
-#pragma unroll
-            for (int e = 0; e < DPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
-        } else {
-#pragma unroll
-            for (int e = 0; e < DPT; ++e) x[e] = 0.f;
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        // any scale and inverse serve: the pieces represent x * inv exactly (up
-        // to the third piece's rounding) and the attention kernel multiplies by sq
-        const float sq = (amax > 0.f) ? amax * (1.f / 448.f) : 1.f;
-        const float inv = __fdividef(1.f, sq);
-#pragma unroll
-        for (int e = 0; e < DPT; ++e) x[e] *= inv;
-        uint8_t* dst = p.qp + (static_cast<size_t>(h) * p.nmt + mt) * kQPieces * (kMTile * D);
-#pragma unroll
-        for (int pc = 0; pc < kQPieces; ++pc) {
-            uint32_t w[DPT / 4];
-#pragma unroll
-            for (int k = 0; k < DPT / 4; ++k) {
-                const uint32_t lo = e4m3x2(x[4 * k], x[4 * k + 1]);
-                const uint32_t hi = e4m3x2(x[4 * k + 2], x[4 * k + 3]);
-                if (pc + 1 < kQPieces) {
-                    const float2 bl = e4m3x2_to_float2(static_cast<uint16_t>(lo));
-                    const float2 bh = e4m3x2_to_float2(static_cast<uint16_t>(hi));
-                    x[4 * k] -= bl.x;
-                    x[4 * k + 1] -= bl.y;
-                    x[4 * k + 2] -= bh.x;
-                    x[4 * k + 3] -= bh.y;
-                }
-                w[k] = lo | (hi << 16);
-            }
-            uint8_t* tile = dst + pc * (kMTile * D);
-#pragma unroll
-            for (int c = 0; c < DPT / 16; ++c)
-                *reinterpret_cast<uint4*>(tile + ktile_off(rrow, dim0 + 16 * c, D)) =
-                    make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-        if (quarter == 0) p.qs[static_cast<size_t>(h) * rows + row] = sq;
-    }
-}
-
-template <int D>
-static cudaError_t launch_q_prep_d(const QPrepParams& p, cudaStream_t s) {
-    const int rows = p.nmt * kMTile;
-    dim3 grid((rows + kPrepRows - 1) / kPrepRows, (p.H + kPrepHeads - 1) / kPrepHeads);
-    q_prep_kernel<D><<<grid, kPrepThreads, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_q_prep(const QPrepParams& p, int D, cudaStream_t s) {
-    return (D == 128) ? launch_q_prep_d<128>(p, s) : launch_q_prep_d<64>(p, s);
-}
 
 // ---------------------------------------------------------------- K4 attention
 
@@ -237,7 +129,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             mbar_init(&bars[B_O_DONE + i], 1);
         }
         mbar_init(&bars[B_DRAIN], 1);
-        mbar_init(&bars[B_Q_FULL], 1);
         misc[2] = 0u;
         fence_mbar_init();
     }
@@ -251,42 +142,111 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     const uint32_t tmem = misc[0];
 
     auto stage_ptr = [&](int s) { return smem + Lay::kStage0 + s * Lay::kStageBytes; };
+    const uint32_t kv_bytes = Lay::kTile + 1024 + (p.masked ? 512 : 0);
+    auto load_tile = [&](int j) {
+        const int s = j % kStages;
+        uint8_t* st = stage_ptr(s);
+        uint64_t* full = &bars[B_KV_FULL + s];
+        mbar_arrive_expect_tx(full, kv_bytes);
+        bulk_g2s(st, p.kc + (static_cast<size_t>(h) * T + j) * Lay::kTile, Lay::kTile, full);
+        bulk_g2s(st + Lay::kTile, p.sk + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
+        bulk_g2s(st + Lay::kTile + 512, p.sv + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
+        if (p.masked) bulk_g2s(st + Lay::kTile + 1024, p.grp + j * kTileSlots, 512, full);
+    };
+    // the first KV tiles are on their way while the queries are prepared
+    if (warp == kWarpLoad && lane == 0)
+        for (int j = 0; j < kStages && j < T; ++j) load_tile(j);
+
+    // ------------------------------------------------------------ query preparation
+    // Each thread takes a quarter (D/4 dims) of query rows tid/4, tid/4 + 96,
+    // ...: RoPE at the row's position, one scale sq = amax/448 per row (any
+    // scale serves: the softmax multiplies it back), and three E4M3 pieces
+    // (hi + mid + lo, ~12 significant bits) of q / sq written into the
+    // swizzled A-operand image; four threads of a row share its amax through
+    // two shuffles.  Rows past n are zero with sq = 1.
+    {
+        constexpr int DPT = D / 4;
+        const int quarter = tid & 3;
+        const int dim0 = quarter * DPT;
+        float* sq_out = reinterpret_cast<float*>(smem + Lay::kSq);
+#pragma unroll 1
+        for (int rr = tid >> 2; rr < kRowsPerCta; rr += kAttnThreads / 4) {  // whole warps leave together
+            const int row = row0 + rr;
+            float x[DPT];
+            float amax = 0.f;
+            if (row < p.n) {
+                uint4 qv[DPT / 8];
+                float4 cs[DPT / 4];  // (cos, sin) of two pairs each
+                const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(row) * p.H + h) * D + dim0);
+                const float4* rsrc =
+                    reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(row) * (D / 2) + dim0 / 2);
+#pragma unroll
+                for (int i = 0; i < DPT / 8; ++i) qv[i] = ldg_nc_na_v4(qsrc + i);
+#pragma unroll
+                for (int i = 0; i < DPT / 4; ++i) cs[i] = __ldg(rsrc + i);
+                const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(qv);
+#pragma unroll
+                for (int j = 0; j < DPT / 2; ++j) {
+                    const float c = (j & 1) ? cs[j >> 1].z : cs[j >> 1].x;
+                    const float sn = (j & 1) ? cs[j >> 1].w : cs[j >> 1].y;
+                    rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), c, sn, x[2 * j],
+                                x[2 * j + 1]);
+                }
+#pragma unroll
+                for (int e = 0; e < DPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPT; ++e) x[e] = 0.f;
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const float sq = (amax > 0.f) ? amax * (1.f / 448.f) : 1.f;
+            const float inv = __fdividef(1.f, sq);
+#pragma unroll
+            for (int e = 0; e < DPT; ++e) x[e] *= inv;
+#pragma unroll
+            for (int pc = 0; pc < kQPieces; ++pc) {
+                uint32_t w[DPT / 4];
+#pragma unroll
+                for (int k = 0; k < DPT / 4; ++k) {
+                    const uint32_t lo = e4m3x2(x[4 * k], x[4 * k + 1]);
+                    const uint32_t hi = e4m3x2(x[4 * k + 2], x[4 * k + 3]);
+                    if (pc + 1 < kQPieces) {
+                        const float2 bl = e4m3x2_to_float2(static_cast<uint16_t>(lo));
+                        const float2 bh = e4m3x2_to_float2(static_cast<uint16_t>(hi));
+                        x[4 * k] -= bl.x;
+                        x[4 * k + 1] -= bl.y;
+                        x[4 * k + 2] -= bh.x;
+                        x[4 * k + 3] -= bh.y;
+                    }
+                    w[k] = lo | (hi << 16);
+                }
+                uint8_t* tile = smem + Lay::kQ + (pc * 2 + (rr >> 7)) * (kMTile * D);
+#pragma unroll
+                for (int c = 0; c < DPT / 16; ++c)
+                    *reinterpret_cast<uint4*>(tile + ktile_off(rr & (kMTile - 1), dim0 + 16 * c, D)) =
+                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            }
+            if (quarter == 0) sq_out[rr] = sq;
+        }
+        fence_async_smem();  // the tensor core reads the pieces through the async proxy
+    }
+    __syncthreads();
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
-            // the prepared query pieces and their row scales
-            uint64_t* qf = &bars[B_Q_FULL];
-            mbar_arrive_expect_tx(qf, kQPieces * 2 * kMTile * D + 2 * kMTile * 4);
-            const int mt0 = blockIdx.x * 2;
-            for (int pc = 0; pc < kQPieces; ++pc)
-                for (int i = 0; i < 2; ++i)
-                    bulk_g2s(smem + Lay::kQ + (pc * 2 + i) * (kMTile * D),
-                             p.qp + ((static_cast<size_t>(h) * p.nmt + mt0 + i) * kQPieces + pc) * (kMTile * D),
-                             kMTile * D, qf);
-            bulk_g2s(smem + Lay::kSq, p.qs + static_cast<size_t>(h) * p.nmt * kMTile + mt0 * kMTile, 2 * kMTile * 4,
-                     qf);
-            const uint32_t bytes = Lay::kTile + 1024 + (p.masked ? 512 : 0);
-            for (int j = 0; j < T; ++j) {
+            // tiles 0 .. kStages-1 went out before the query preparation
+            for (int j = kStages; j < T; ++j) {
                 const int s = j % kStages;
                 if (!mbar_wait(&bars[B_KV_EMPTY + s], ((j / kStages) & 1) ^ 1, ab, kDevTimeoutLoader)) break;
-                uint8_t* st = stage_ptr(s);
-                uint64_t* full = &bars[B_KV_FULL + s];
-                mbar_arrive_expect_tx(full, bytes);
-                bulk_g2s(st, p.kc + (static_cast<size_t>(h) * T + j) * Lay::kTile, Lay::kTile, full);
-                bulk_g2s(st + Lay::kTile, p.sk + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
-                bulk_g2s(st + Lay::kTile + 512, p.sv + static_cast<size_t>(h) * p.Cpad + j * kTileSlots, 512, full);
-                if (p.masked) bulk_g2s(st + Lay::kTile + 1024, p.grp + j * kTileSlots, 512, full);
+                load_tile(j);
             }
             if (*ab.flag) {
-                // leave no copy in flight: wait (bounded) for the query copies and
-                // the last fill of each stage
-                uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&bars[B_Q_FULL], 0) && global_timer_ns() - t0 < 100000000ull) {
-                }
+                // leave no copy in flight: wait (bounded) for the last fill of each stage
                 for (int s = 0; s < kStages && s < T; ++s) {
                     const int last = ((T - 1 - s) / kStages) * kStages + s;
-                    t0 = global_timer_ns();
+                    const uint64_t t0 = global_timer_ns();
                     while (!mbar_try_wait(&bars[B_KV_FULL + s], (last / kStages) & 1) &&
                            global_timer_ns() - t0 < 100000000ull) {
                     }
@@ -322,7 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     mma_f16_ts(d_tmem, a_tmem + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutMma);
+            bool ok = true;
             for (int j = 0; j < T && ok; ++j) {
                 const int s = j % kStages;
                 ok = mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutMma);
@@ -387,8 +347,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         float svmax = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) svmax = fmaxf(svmax, reinterpret_cast<const float*>(misc)[4 + w]);
-        bool ok = warp_wait(&bars[B_Q_FULL], 0, ab, kDevTimeoutSoftmax);
-        const float a = ok ? s_sq[mt * kMTile + r] * p.sm_log2 : 0.f;  // > 0
+        bool ok = true;
+        const float a = s_sq[mt * kMTile + r] * p.sm_log2;  // > 0
         const float lsv = (svmax > 0.f) ? lg2_approx(svmax) : 0.f;
         const float2 a2 = make_float2(a, a);
         float m_run = -INFINITY, l_run = 0.f;
@@ -693,7 +653,7 @@ static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(p.nmt / 2, p.H);
+    dim3 grid((p.n + kRowsPerCta - 1) / kRowsPerCta, p.H);
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

@@ -61,9 +61,6 @@ struct rc_cache {
     uint8_t* d_rt_vt = nullptr;
     float* d_rt_sk = nullptr;
     float* d_rt_sv = nullptr;
-    uint8_t* d_qp = nullptr;   // prepared query pieces of one attention call
-    float* d_qs = nullptr;     // their row scales
-    int nmt_max = 0;           // 128-row query tiles for max_write queries (even)
     RopeEntry pool[kPoolEntries];
     uint64_t clock = 0;
     // host mirrors of the ring tables
@@ -111,8 +108,6 @@ void free_all(rc_cache* h) {
     cudaFree(h->d_rt_vt);
     cudaFree(h->d_rt_sk);
     cudaFree(h->d_rt_sv);
-    cudaFree(h->d_qp);
-    cudaFree(h->d_qs);
     for (auto& e : h->pool) {
         cudaFree(e.d_table);
         cudaFree(e.d_pos);
@@ -276,9 +271,6 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     st |= dmalloc(&h->d_grp, static_cast<size_t>(h->L) * h->Cpad);
     st |= dmalloc(&h->d_theta, static_cast<size_t>(h->D / 2));
     st |= dmalloc(&h->d_status, 1);
-    h->nmt_max = 2 * ((h->max_write + 255) / 256);
-    st |= dmalloc(&h->d_qp, static_cast<size_t>(h->H) * h->nmt_max * 3 * 128 * h->D);
-    st |= dmalloc(&h->d_qs, static_cast<size_t>(h->H) * h->nmt_max * 128);
     for (auto& e : h->pool) {
         st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
         st |= dmalloc(&e.d_pos, static_cast<size_t>(h->max_write));
@@ -518,21 +510,6 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
         ap.sv = h->d_sv + lsc;
     }
     ap.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
-    // query preparation: rotated, scaled, split into E4M3 pieces in the
-    // attention kernel's shared-memory layout
-    QPrepParams qp{};
-    qp.q = static_cast<const __nv_bfloat16*>(Q_bf16);
-    qp.rope = h->pool[entry].d_table;
-    qp.qp = h->d_qp;
-    qp.qs = h->d_qs;
-    qp.n = n;
-    qp.H = h->H;
-    qp.nmt = 2 * ((n + 255) / 256);
-    if (launch_q_prep(qp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
-    h->launches += 1;
-    ap.qp = h->d_qp;
-    ap.qs = h->d_qs;
-    ap.nmt = qp.nmt;
     ap.q = static_cast<const __nv_bfloat16*>(Q_bf16);
     ap.rope = h->pool[entry].d_table;
     ap.out = out;

@@ -69,13 +69,6 @@ struct ReadtimeParams {
 // one fp32 scale per (token, head) row, three E4M3 pieces per element laid out
 // as the swizzled shared-memory image of the attention kernel's A operand;
 // and the largest V scale of every head.
-struct QPrepParams {
-    const __nv_bfloat16* q;  // [n][H][D]
-    const float2* rope;      // [n][D/2]
-    uint8_t* qp;             // [H][nmt][3][128][D] (rows >= n are zero)
-    float* qs;               // [H][nmt * 128] row scales (1 for rows >= n)
-    int n, H, nmt;           // nmt: 128-row M tiles, rounded up to even
-};
 
 // K4: FP8 attention over one layer's ring.
 struct AttnParams {
@@ -87,9 +80,6 @@ struct AttnParams {
     const __nv_bfloat16* q;  // [n][H][D]
     const float2* rope;    // [n][D/2]
     float* out;            // [n][H][D]
-    const uint8_t* qp;     // prepared query pieces (QPrepParams::qp)
-    const float* qs;       // row scales
-    int nmt;               // M tiles in qp / qs (even)
     int n, H, C, T, Cpad;
     int masked;            // 1: some slots are empty, read grp
     // bit j: every ring slot of KV tile j (the last tile may hold fewer than
@@ -104,7 +94,6 @@ cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t s);
 cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s);
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status);
 cudaError_t launch_readtime(const ReadtimeParams& p, int D, cudaStream_t s);
-cudaError_t launch_q_prep(const QPrepParams& p, int D, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, cudaStream_t s);
 
 // Status values a kernel writes into the device status word.
