@@ -82,6 +82,14 @@ struct AttnLayout {
 
 // ---------------------------------------------------------------- K4 attention
 
+// x rounded to 4 significant bits (Veltkamp's splitting with 2^20 + 1 on a
+// 24-bit significand): an E4M3 value whenever |x| lies in E4M3's normal
+// range, and x - split4(x) is exact.  Plain multiply and subtract, never fused.
+__device__ __forceinline__ float split4(float x) {
+    const float c = __fmul_rn(x, 1048577.0f);
+    return __fsub_rn(c, __fsub_rn(c, x));
+}
+
 // Every lane waits; the warp continues only if all lanes saw the phase.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState ab, int where) {
     const bool ok = mbar_wait(bar, parity, ab, where);
@@ -158,39 +166,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         for (int j = 0; j < kStages && j < T; ++j) load_tile(j);
 
     // ------------------------------------------------------------ query preparation
-    // Each thread takes a quarter (D/4 dims) of query rows tid/4, tid/4 + 96,
-    // ...: RoPE at the row's position, one scale sq = amax/448 per row (any
-    // scale serves: the softmax multiplies it back), and three E4M3 pieces
-    // (hi + mid + lo, ~12 significant bits) of q / sq written into the
-    // swizzled A-operand image; four threads of a row share its amax through
-    // two shuffles.  Rows past n are zero with sq = 1.
+    // The CTA's bf16 query rows are first copied (cp.async, 16-byte pieces
+    // XOR-swizzled by row) into the fp16 V buffers, which the converter fills
+    // only after this prologue.  Then each thread takes a quarter of query rows
+    // tid/4, tid/4 + 96, ... -- dims 16j + 4q .. 16j + 4q + 3 (q = tid % 4), so
+    // that the four threads of a row read its cos/sin in 64 contiguous bytes --
+    // with the next row's cos/sin loads in flight while one computes: RoPE at
+    // the row's position, one scale sq = amax/448 per row (any scale serves: the
+    // softmax multiplies it back), and three E4M3 pieces (hi + mid + lo, ~12
+    // significant bits) of q / sq written into the swizzled A-operand image.
+    // Rows past n are zero with sq = 1.
     {
-        constexpr int DPT = D / 4;
+        constexpr int DPT = D / 4;                                        // dims per thread
+        constexpr int kGroups = DPT / 4;                                  // 4-dim groups per thread
+        constexpr int kUnits = D * 2 / 16;                                // 16-byte pieces of a bf16 row
+        constexpr int kRowStep = kAttnThreads / 4;                        // rows per pass
+        constexpr int kPasses = (kRowsPerCta + kRowStep - 1) / kRowStep;
+        uint8_t* qstage = smem + Lay::kV16;                               // [256 rows][D] bf16
+        static_assert(kRowsPerCta * D * 2 <= Lay::kV16Bytes, "query rows do not fit the V buffers");
+        const int rows_here = min(kRowsPerCta, p.n - row0);
+        for (int u = tid; u < rows_here * kUnits; u += kAttnThreads) {
+            const int rr = u / kUnits, c = u - rr * kUnits;
+            cp_async16(qstage + rr * (D * 2) + ((c ^ (rr & 7)) << 4),
+                       p.q + (static_cast<size_t>(row0 + rr) * p.H + h) * D + c * 8);
+        }
         const int quarter = tid & 3;
-        const int dim0 = quarter * DPT;
         float* sq_out = reinterpret_cast<float*>(smem + Lay::kSq);
-#pragma unroll 1
-        for (int rr = tid >> 2; rr < kRowsPerCta; rr += kAttnThreads / 4) {  // whole warps leave together
+        float4 cs[2][kGroups];  // group j: (cos, sin) of dims 16j + 4q + {0,1} and {2,3}
+        auto load_rope = [&](int ps, int buf) {
+            const int rr = (tid >> 2) + ps * kRowStep;
+            const int row = row0 + rr;
+            if (rr < kRowsPerCta && row < p.n) {
+                const float4* rsrc = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(row) * (D / 2));
+#pragma unroll
+                for (int j = 0; j < kGroups; ++j) cs[buf][j] = __ldg(rsrc + 4 * j + quarter);
+            }
+        };
+        load_rope(0, 0);
+        cp_async_wait_all();
+        __syncthreads();
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int buf = ps & 1;
+            if (ps + 1 < kPasses) load_rope(ps + 1, buf ^ 1);
+            const int rr = (tid >> 2) + ps * kRowStep;
+            if (rr >= kRowsPerCta) break;  // whole warps leave together
             const int row = row0 + rr;
             float x[DPT];
             float amax = 0.f;
             if (row < p.n) {
-                uint4 qv[DPT / 8];
-                float4 cs[DPT / 4];  // (cos, sin) of two pairs each
-                const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(row) * p.H + h) * D + dim0);
-                const float4* rsrc =
-                    reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(row) * (D / 2) + dim0 / 2);
 #pragma unroll
-                for (int i = 0; i < DPT / 8; ++i) qv[i] = ldg_nc_na_v4(qsrc + i);
-#pragma unroll
-                for (int i = 0; i < DPT / 4; ++i) cs[i] = __ldg(rsrc + i);
-                const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(qv);
-#pragma unroll
-                for (int j = 0; j < DPT / 2; ++j) {
-                    const float c = (j & 1) ? cs[j >> 1].z : cs[j >> 1].x;
-                    const float sn = (j & 1) ? cs[j >> 1].w : cs[j >> 1].y;
-                    rotate_pair(__bfloat162float(qb[2 * j]), __bfloat162float(qb[2 * j + 1]), c, sn, x[2 * j],
-                                x[2 * j + 1]);
+                for (int j = 0; j < kGroups; ++j) {
+                    // dims 16j + 4q .. +3: 8 bytes in piece 2j + q/2 of the row
+                    const uint2 qq = *reinterpret_cast<const uint2*>(
+                        qstage + rr * (D * 2) + (((2 * j + (quarter >> 1)) ^ (rr & 7)) << 4) + (quarter & 1) * 8);
+                    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qq);
+                    rotate_pair(__bfloat162float(qb[0]), __bfloat162float(qb[1]), cs[buf][j].x, cs[buf][j].y,
+                                x[4 * j], x[4 * j + 1]);
+                    rotate_pair(__bfloat162float(qb[2]), __bfloat162float(qb[3]), cs[buf][j].z, cs[buf][j].w,
+                                x[4 * j + 2], x[4 * j + 3]);
                 }
 #pragma unroll
                 for (int e = 0; e < DPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
@@ -206,26 +240,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             for (int e = 0; e < DPT; ++e) x[e] *= inv;
 #pragma unroll
             for (int pc = 0; pc < kQPieces; ++pc) {
-                uint32_t w[DPT / 4];
-#pragma unroll
-                for (int k = 0; k < DPT / 4; ++k) {
-                    const uint32_t lo = e4m3x2(x[4 * k], x[4 * k + 1]);
-                    const uint32_t hi = e4m3x2(x[4 * k + 2], x[4 * k + 3]);
-                    if (pc + 1 < kQPieces) {
-                        const float2 bl = e4m3x2_to_float2(static_cast<uint16_t>(lo));
-                        const float2 bh = e4m3x2_to_float2(static_cast<uint16_t>(hi));
-                        x[4 * k] -= bl.x;
-                        x[4 * k + 1] -= bl.y;
-                        x[4 * k + 2] -= bh.x;
-                        x[4 * k + 3] -= bh.y;
-                    }
-                    w[k] = lo | (hi << 16);
-                }
                 uint8_t* tile = smem + Lay::kQ + (pc * 2 + (rr >> 7)) * (kMTile * D);
 #pragma unroll
-                for (int c = 0; c < DPT / 16; ++c)
-                    *reinterpret_cast<uint4*>(tile + ktile_off(rr & (kMTile - 1), dim0 + 16 * c, D)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                for (int j = 0; j < kGroups; ++j) {
+                    float y[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // all pieces but the last: x to 4 significant bits (an
+                        // E4M3 value), and the exact remainder carries on
+                        y[e] = (pc + 1 < kQPieces) ? split4(x[4 * j + e]) : x[4 * j + e];
+                        if (pc + 1 < kQPieces) x[4 * j + e] = __fsub_rn(x[4 * j + e], y[e]);
+                    }
+                    *reinterpret_cast<uint32_t*>(tile + ktile_off(rr & (kMTile - 1), 16 * j + 4 * quarter, D)) =
+                        e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+                }
             }
             if (quarter == 0) sq_out[rr] = sq;
         }
