@@ -310,31 +310,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     mma_f16_ts(d_tmem, a_tmem + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
+            // A wait polls an mbarrier in shared memory, which the tensor core's
+            // operand reads keep busy: each is placed right after an issue, so
+            // it overlaps MMAs already queued.  Per tile j: PV0(j-1), [K tile
+            // j], QK0(j), [P1], PV1(j-1), QK1(j), [next tile's fp16 V].
+            auto v16_ready = [&](int jt) {
+                return mbar_wait(&bars[B_V16_FULL + (jt & 1)], (jt >> 1) & 1, ab, kDevTimeoutMma);
+            };
             bool ok = true;
             for (int j = 0; j < T && ok; ++j) {
                 const int s = j % kStages;
-                ok = mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutMma);
-                if (!ok) break;
-                tc_fence_after();
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (j > 0) {
                         ok = mbar_wait(&bars[B_P_FULL + i], (j - 1) & 1, ab, kDevTimeoutMma);
-                        if (ok && i == 0)
-                            ok = mbar_wait(&bars[B_V16_FULL + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kDevTimeoutMma);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(i, j - 1, j - 1 > 0);
                         if (i == 1) mma_commit(&bars[B_V16_EMPTY + ((j - 1) & 1)]);
                     }
+                    if (i == 0) {
+                        ok = mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutMma);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
                     issue_qk(i, s);
                     mma_commit(&bars[B_S_FULL + i]);
                 }
                 if (ok) mma_commit(&bars[B_KV_EMPTY + s]);
+                if (ok) ok = v16_ready(j);  // for PV0(j) in the next round
             }
             for (int i = 0; i < 2 && ok; ++i) {
                 ok = mbar_wait(&bars[B_P_FULL + i], (T - 1) & 1, ab, kDevTimeoutMma);
-                if (ok && i == 0)
-                    ok = mbar_wait(&bars[B_V16_FULL + ((T - 1) & 1)], ((T - 1) >> 1) & 1, ab, kDevTimeoutMma);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(i, T - 1, T - 1 > 0);
