@@ -45,8 +45,8 @@ TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
     # the production call (ncu, profiles/attn_kernel_production_call.md), valid
     # while rc_attention.cu has this hash
-    "attention": {"bytes": 92.70e6,
-                  "src_sha256": "98043bc625d0c459ba2cf08e96058fdf2679447a146448934536327344d1cfa5"},
+    "attention": {"bytes": 87.55e6,
+                  "src_sha256": "e61bc235f51ffa950e198625efcb0e42023ec9f047a3c90a6f6079ecabacd79f"},
 }
 
 
