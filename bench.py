@@ -46,7 +46,7 @@ TRAFFIC = {
     # the production call (ncu, profiles/attn_kernel_production_call.md), valid
     # while rc_attention.cu has this hash
     "attention": {"bytes": 87.55e6,
-                  "src_sha256": "e61bc235f51ffa950e198625efcb0e42023ec9f047a3c90a6f6079ecabacd79f"},
+                  "src_sha256": "33f2d9ff2c715b7c6f7f457510b7dbcb5daf96d0c88f91edb8b606432220b906"},
 }
 
 

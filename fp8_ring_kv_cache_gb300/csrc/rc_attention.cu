@@ -78,8 +78,6 @@ struct AttnLayout {
     static constexpr uint32_t kAlloc = kTotal + 1024;  // room to align the base to 1024
 };
 
-// ---------------------------------------------------------------- K6 query preparation
-
 // ---------------------------------------------------------------- K4 attention
 
 // x rounded to 4 significant bits (Veltkamp's splitting with 2^20 + 1 on a

@@ -65,12 +65,8 @@ struct ReadtimeParams {
     int H, C, T, Cpad;
 };
 
-// K6: query preparation for one attention call: RoPE at the query positions,
-// one fp32 scale per (token, head) row, three E4M3 pieces per element laid out
-// as the swizzled shared-memory image of the attention kernel's A operand;
-// and the largest V scale of every head.
-
-// K4: FP8 attention over one layer's ring.
+// K4: FP8 attention over one layer's ring (the queries are rotated, scaled
+// and split into E4M3 pieces in the kernel's prologue).
 struct AttnParams {
     const uint8_t* kc;     // layer [H][T][128][D]
     const uint8_t* vt;     // layer [H][T][D][128]
