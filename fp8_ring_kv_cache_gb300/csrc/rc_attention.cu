@@ -21,7 +21,12 @@
 //   softmax: score = S * sq_row * sk_slot * log2(e)/sqrt(D); online max and sum
 //         in registers (packed fp32x2 arithmetic, lazy rescaling of O);
 //         P = exp2(score - max) * sv_slot / max(sv) -> fp16, written back over
-//         S in TMEM.
+//         S in TMEM.  Three paths by the tile's write groups (the host marks
+//         them per tile): one group (one K and one V scale, all in
+//         registers), two runs [0, b) and [b, 128) (a write's run of slots
+//         ends inside the tile; two scale pairs, all in registers), anything
+//         else (per-column scales and validity, out of line: rare on a full
+//         ring).
 //   O_i += P_i V_j on tcgen05 kind::f16 with P read from TMEM (A operand) and
 //         the converted V tile from shared memory (B operand).
 // Two M tiles ping-pong so the tensor pipe works on one tile while the other
@@ -102,6 +107,89 @@ __device__ __forceinline__ void e4m3x4_to_f16x4_div256(uint32_t w, uint32_t& lo,
     const uint32_t b = __byte_perm(w, 0u, 0x3424);  // codes 2, 3 in bytes 1 and 3
     lo = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
     hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
+}
+
+// Softmax of any other tile (per-column scales, and on a masked tile or one
+// the ring ends inside, a validity test): pass A and pass B each read the
+// scores from TMEM in 32-column chunks.  Rare on a full ring, so it is kept
+// out of line and the hot loop stays small.  Returns (new running max, rescale
+// factor of the old one, the tile's row sum); P goes to TMEM columns 0..63.
+__device__ __noinline__ float3 general_tile_softmax(uint32_t s_tm, const float* ssk, const float* ssv,
+                                                    const int32_t* sgrp, int masked, int nvalid, float a, float lsv,
+                                                    float m_run) {
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    // validity of four columns as selects; all of a chunk's scale (and group)
+    // loads are issued together, none sits behind a branch
+    auto ok4 = [&](int col, bool (&ok)[4]) {
+        const int4 g4 = masked ? *reinterpret_cast<const int4*>(sgrp + col) : make_int4(0, 0, 0, 0);
+        ok[0] = (col < nvalid) && g4.x >= 0;
+        ok[1] = (col + 1 < nvalid) && g4.y >= 0;
+        ok[2] = (col + 2 < nvalid) && g4.z >= 0;
+        ok[3] = (col + 3 < nvalid) && g4.w >= 0;
+    };
+    auto max_chunk = [&](const uint32_t (&v)[32], int c) {
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+            const int col = 32 * c + k;
+            const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
+            bool ok[4];
+            ok4(col, ok);
+            const float2 y0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), make_float2(s4.x, s4.y));
+            const float2 y1 =
+                mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), make_float2(s4.z, s4.w));
+            mx[(k >> 2) & 1] = max3(mx[(k >> 2) & 1], ok[0] ? y0.x : -INFINITY, ok[1] ? y0.y : -INFINITY);
+            mx[2 + ((k >> 2) & 1)] = max3(mx[2 + ((k >> 2) & 1)], ok[2] ? y1.x : -INFINITY, ok[3] ? y1.y : -INFINITY);
+        }
+    };
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(s_tm + 32 * c, v);
+        max_chunk(v, c);
+    }
+    const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
+    const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+    const float m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+    const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = bump ? ex2(m_run - m_fin) : 1.f;
+    const float msub = m_fin + lsv;
+    const float2 a2 = make_float2(a, a), nm2 = make_float2(-msub, -msub);
+    float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+    // P' = exp2(S sk a - m - log2(max sv)) * sv; the row sum leaves sv out
+    auto p_chunk = [&](const uint32_t (&v)[32], int c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+            const int col = 32 * c + k;
+            const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
+            const float4 v4 = *reinterpret_cast<const float4*>(ssv + col);
+            bool ok[4];
+            ok4(col, ok);
+            const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                                        make_float2(s4.x, s4.y)), a2, nm2);
+            const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                                        make_float2(s4.z, s4.w)), a2, nm2);
+            const float2 p0 = make_float2(ok[0] ? ex2(x0.x) : 0.f, ok[1] ? ex2(x0.y) : 0.f);
+            const float2 p1 = make_float2(ok[2] ? ex2(x1.x) : 0.f, ok[3] ? ex2(x1.y) : 0.f);
+            ls0 = add2(ls0, p0);
+            ls1 = add2(ls1, p1);
+            const float2 q0 = make_float2(ok[0] ? p0.x * v4.x : 0.f, ok[1] ? p0.y * v4.y : 0.f);
+            const float2 q1 = make_float2(ok[2] ? p1.x * v4.z : 0.f, ok[3] ? p1.y * v4.w : 0.f);
+            __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+            __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+            pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
+            pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+        }
+        // P chunk c goes to columns 16c..16c+15, which were read in chunks <= c
+        tmem_st16(s_tm + 16 * c, pk);
+    };
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(s_tm + 32 * c, v);
+        p_chunk(v, c);
+    }
+    return make_float3(m_new, alpha, (ls0.x + ls0.y) + (ls1.x + ls1.y));
 }
 
 template <int D>
@@ -480,91 +568,114 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     tmem_st32(s_tm, pa);
                     tmem_st32(s_tm + 32, pb);
             };
-            if (uni && nvalid == kTileSlots) {
-                uniform_tile(std::false_type{});
-            } else if (uni) {
-                uniform_tile(std::true_type{});
-            } else {
-                // Per-column scales (and, on a partial or masked tile, a validity
-                // test): pass A and pass B each read the scores from TMEM in
-                // 32-column chunks.
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                // validity of four columns as selects; all of a chunk's scale (and
-                // group) loads are issued together, none sits behind a branch
-                auto ok4 = [&](int col, bool (&ok)[4]) {
-                    const int4 g4 = p.masked ? *reinterpret_cast<const int4*>(sgrp + col) : make_int4(0, 0, 0, 0);
-                    ok[0] = (col < nvalid) && g4.x >= 0;
-                    ok[1] = (col + 1 < nvalid) && g4.y >= 0;
-                    ok[2] = (col + 2 < nvalid) && g4.z >= 0;
-                    ok[3] = (col + 3 < nvalid) && g4.w >= 0;
-                };
-                auto max_chunk = [&](const uint32_t (&v)[32], int c) {
+            // Split tile: slots [0, sb) belong to one write group (scales A) and
+            // [sb, 128) to another (B), as where a write's run of slots ends
+            // inside a tile.  The 32-column chunk holding column sb is loaded
+            // into v3 and the other three into v0..v2, in order: those three run
+            // the uniform arithmetic with their chunk's scales, v3 selects A or B
+            // per column.  One TMEM round trip, no per-column scale loads.
+            auto split_tile = [&](int sb) {
+                const int cs = sb >> 5;                   // the chunk holding column sb
+                const int eb = sb - 32 * cs;              // its columns in group A: 0..31
+                const int c0 = cs > 0 ? 0 : 1, c1 = cs > 1 ? 1 : 2, c2 = cs > 2 ? 2 : 3;
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32_async(s_tm + 32 * c0, v0);
+                tmem_ld32_async(s_tm + 32 * c1, v1);
+                tmem_ld32_async(s_tm + 32 * c2, v2);
+                tmem_ld32_async(s_tm + 32 * cs, v3);
+                const float cuA = ssk[0] * a, cuB = ssk[kTileSlots - 1] * a;
+                const float lvA = lg2_approx(ssv[0]), lvB = lg2_approx(ssv[kTileSlots - 1]);
+                tmem_wait_ld_dep(v0);
+                reg_fence(v1);
+                reg_fence(v2);
+                reg_fence(v3);
+                auto cmax = [](const uint32_t (&v)[32]) {
+                    float t[11];
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const int col = 32 * c + k;
-                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
-                        bool ok[4];
-                        ok4(col, ok);
-                        const float2 y0 = mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                               make_float2(s4.x, s4.y));
-                        const float2 y1 = mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                               make_float2(s4.z, s4.w));
-                        mx[(k >> 2) & 1] =
-                            max3(mx[(k >> 2) & 1], ok[0] ? y0.x : -INFINITY, ok[1] ? y0.y : -INFINITY);
-                        mx[2 + ((k >> 2) & 1)] =
-                            max3(mx[2 + ((k >> 2) & 1)], ok[2] ? y1.x : -INFINITY, ok[3] ? y1.y : -INFINITY);
-                    }
+                    for (int i = 0; i < 10; ++i)
+                        t[i] = max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                                    __uint_as_float(v[3 * i + 2]));
+                    t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+                    const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
+                    const float u2 = max3(t[6], t[7], t[8]), u3 = max3(t[9], t[10], u0);
+                    return max3(u1, u2, u3);
                 };
-                // rare (partial, masked or mixed-group tiles): a compact loop, one
-                // chunk at a time
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(s_tm + 32 * c, v);
-                    max_chunk(v, c);
+                // the scales are positive, so a chunk's max scales with its group's factor
+                float mA = -INFINITY, mB = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float x0 = __uint_as_float(v3[k]), x1 = __uint_as_float(v3[k + 1]);
+                    mA = max3(mA, k < eb ? x0 : -INFINITY, k + 1 < eb ? x1 : -INFINITY);
+                    mB = max3(mB, k < eb ? -INFINITY : x0, k + 1 < eb ? -INFINITY : x1);
                 }
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a;
+                const float m_tile =
+                    fmaxf(fmaxf(cmax(v0) * (cs > 0 ? cuA : cuB), cmax(v1) * (cs > 1 ? cuA : cuB)),
+                          fmaxf(cmax(v2) * (cs > 2 ? cuA : cuB), fmaxf(mA * cuA, mB * cuB)));
                 const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
                 m_new = bump ? fmaxf(m_run, m_tile) : m_run;
                 const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
                 alpha = bump ? ex2(m_run - m_fin) : 1.f;
                 const float msub = m_fin + lsv;
-                const float2 nm2 = make_float2(-msub, -msub);
-                auto p_chunk = [&](const uint32_t (&v)[32], int c) {
+                const float nmA = lvA - msub, nmB = lvB - msub;
+                const float isvA = ex2(-lvA), isvB = ex2(-lvB);
+                // P' = exp2(S c - m - log2(max sv) + log2(sv)); the row sum takes each
+                // group's V scale back out
+                auto p_one = [&](const uint32_t (&v)[32], int c, bool ga) {
+                    const float2 c2 = ga ? make_float2(cuA, cuA) : make_float2(cuB, cuB);
+                    const float2 n2 = ga ? make_float2(nmA, nmA) : make_float2(nmB, nmB);
+                    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
                     uint32_t pk[16];
 #pragma unroll
                     for (int k = 0; k < 32; k += 4) {
-                        const int col = 32 * c + k;
-                        const float4 s4 = *reinterpret_cast<const float4*>(ssk + col);
-                        const float4 v4 = *reinterpret_cast<const float4*>(ssv + col);
-                        bool ok[4];
-                        ok4(col, ok);
-                        const float2 x0 = fma2(mul2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                                                    make_float2(s4.x, s4.y)), a2, nm2);
-                        const float2 x1 = fma2(mul2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                                                    make_float2(s4.z, s4.w)), a2, nm2);
-                        const float2 p0 = make_float2(ok[0] ? ex2(x0.x) : 0.f, ok[1] ? ex2(x0.y) : 0.f);
-                        const float2 p1 = make_float2(ok[2] ? ex2(x1.x) : 0.f, ok[3] ? ex2(x1.y) : 0.f);
-                        ls[0] = add2(ls[0], p0);
-                        ls[1] = add2(ls[1], p1);
-                        const float2 q0 =
-                            make_float2(ok[0] ? p0.x * v4.x : 0.f, ok[1] ? p0.y * v4.y : 0.f);
-                        const float2 q1 =
-                            make_float2(ok[2] ? p1.x * v4.z : 0.f, ok[3] ? p1.y * v4.w : 0.f);
+                        const float2 x0 = fma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), c2, n2);
+                        const float2 x1 =
+                            fma2(make_float2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), c2, n2);
+                        const float2 q0 = make_float2(ex2(x0.x), ex2(x0.y));
+                        const float2 q1 = make_float2(ex2(x1.x), ex2(x1.y));
+                        s0 = add2(s0, q0);
+                        s1 = add2(s1, q1);
                         __half2 h0 = __floats2half2_rn(q0.x, q0.y);
                         __half2 h1 = __floats2half2_rn(q1.x, q1.y);
                         pk[k / 2] = *reinterpret_cast<uint32_t*>(&h0);
                         pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
                     }
-                    // P chunk c goes to columns 16c..16c+15, which were read in chunks <= c
+                    ls[0].x += ((s0.x + s0.y) + (s1.x + s1.y)) * (ga ? isvA : isvB);
+                    // P of chunk c goes to columns 16c..16c+15 (every score is in registers)
                     tmem_st16(s_tm + 16 * c, pk);
                 };
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(s_tm + 32 * c, v);
-                    p_chunk(v, c);
+                p_one(v0, c0, cs > 0);
+                p_one(v1, c1, cs > 1);
+                p_one(v2, c2, cs > 2);
+                {
+                    float2 sw = make_float2(0.f, 0.f);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const bool a0 = k < eb, a1 = k + 1 < eb;
+                        const float2 x = fma2(make_float2(__uint_as_float(v3[k]), __uint_as_float(v3[k + 1])),
+                                              make_float2(a0 ? cuA : cuB, a1 ? cuA : cuB),
+                                              make_float2(a0 ? nmA : nmB, a1 ? nmA : nmB));
+                        const float2 q = make_float2(ex2(x.x), ex2(x.y));
+                        sw = fma2(q, make_float2(a0 ? isvA : isvB, a1 ? isvA : isvB), sw);
+                        __half2 hq = __floats2half2_rn(q.x, q.y);
+                        pk[k / 2] = *reinterpret_cast<uint32_t*>(&hq);
+                    }
+                    ls[0].y += sw.x + sw.y;
+                    tmem_st16(s_tm + 16 * cs, pk);
                 }
+            };
+            const int sb = uni ? 0 : static_cast<int>(p.split[j]);
+            if (__builtin_expect(uni && nvalid == kTileSlots, 1)) {
+                uniform_tile(std::false_type{});
+            } else if (uni) {
+                uniform_tile(std::true_type{});
+            } else if (sb != 0) {
+                split_tile(sb);
+            } else {
+                const float3 r = general_tile_softmax(s_tm, ssk, ssv, sgrp, p.masked, nvalid, a, lsv, m_run);
+                m_new = r.x;
+                alpha = r.y;
+                ls[0].x = r.z;
             }
             tmem_st_wait();
             __syncwarp();
@@ -582,6 +693,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 tmem_st_wait();
             }
             // on uniform tiles the sum holds P' = P'' * 2^log2(sv): take the V scale back out
+            // (split tiles weight their sums per group, with isv0 = 1)
             const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
             l_run = l_run * alpha + lsum * isv0;
             m_run = m_new;

@@ -71,6 +71,7 @@ struct rc_cache {
     std::vector<std::vector<int64_t>> last_pos;          // per layer
     std::vector<int> last_n, last_entry;
     std::vector<std::array<uint64_t, 4>> uniform;  // per layer: tiles inside one write group
+    std::vector<std::array<uint8_t, 256>> split;   // per layer: two-run tiles (first slot of the second run)
     std::vector<char> uniform_dirty;
     std::vector<uint32_t> slot_mark;
     uint32_t mark = 0;
@@ -117,19 +118,30 @@ void free_all(rc_cache* h) {
     delete h;
 }
 
-// Tiles whose 128 slots are all occupied by a single write group.
+// Tiles whose slots are all occupied by a single write group (uniform), and
+// full tiles made of two runs, slots [0, b) of one write group and [b, 128) of
+// another (split[t] = b, 1..127; 0 for every other tile).
 void refresh_uniform(rc_cache* h, int layer) {
     if (!h->uniform_dirty[layer]) return;
     auto& m = h->uniform[layer];
+    auto& sp = h->split[layer];
     m = {0, 0, 0, 0};
+    sp.fill(0);
     const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
     for (int t = 0; t < h->T && t < 256; ++t) {
         // the ring's slots of the tile (the last tile may end before 128)
         const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, h->C);
         if (g[s0] < 0) continue;
-        bool same = true;
-        for (int s = s0 + 1; s < s1 && same; ++s) same = (g[s] == g[s0]);
-        if (same) m[t >> 6] |= 1ull << (t & 63);
+        int b = s0 + 1;
+        while (b < s1 && g[b] == g[s0]) ++b;
+        if (b == s1) {
+            m[t >> 6] |= 1ull << (t & 63);
+            continue;
+        }
+        if (s1 - s0 != kTileSlots || g[b] < 0) continue;
+        int e = b + 1;
+        while (e < s1 && g[e] == g[b]) ++e;
+        if (e == s1) sp[t] = static_cast<uint8_t>(b - s0);
     }
     h->uniform_dirty[layer] = 0;
 }
@@ -303,6 +315,11 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
         const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
         ok = cudaMemset(h->d_kraw, 0, raw * 2) == cudaSuccess && cudaMemset(h->d_vraw, 0, raw * 2) == cudaSuccess &&
              cudaMemset(h->d_slot_rope, 0, sizeof(float2) * h->L * h->Cpad * (h->D / 2)) == cudaSuccess;
+        // the read-time ring's padding slots, like the main ring's, hold zero codes
+        const size_t one = static_cast<size_t>(h->H) * h->T * kTileSlots * h->D;
+        ok = ok && cudaMemset(h->d_rt_kc, 0, one) == cudaSuccess && cudaMemset(h->d_rt_vt, 0, one) == cudaSuccess &&
+             cudaMemset(h->d_rt_sk, 0, sizeof(float) * h->H * h->Cpad) == cudaSuccess &&
+             cudaMemset(h->d_rt_sv, 0, sizeof(float) * h->H * h->Cpad) == cudaSuccess;
     }
     h->theta.resize(h->D / 2);
     for (int i = 0; i < h->D / 2; ++i) h->theta[i] = std::pow(cfg->rope_base, -2.0 * i / h->D);
@@ -329,6 +346,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     h->last_n.assign(h->L, 0);
     h->last_entry.assign(h->L, -1);
     h->uniform.assign(h->L, std::array<uint64_t, 4>{0, 0, 0, 0});
+    h->split.assign(h->L, std::array<uint8_t, 256>{});
     h->uniform_dirty.assign(h->L, 1);
     h->slot_mark.assign(h->C, 0);
     *out = h;
@@ -529,9 +547,11 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
             for (int s = s0; s < s1 && occ; ++s) occ = (g[s] >= 0);
             if (occ) ap.uniform[t >> 6] |= 1ull << (t & 63);
         }
+        std::memset(ap.split, 0, sizeof(ap.split));
     } else {
         refresh_uniform(h, layer);
         for (int w = 0; w < 4; ++w) ap.uniform[w] = h->uniform[layer][w];
+        std::memcpy(ap.split, h->split[layer].data(), sizeof(ap.split));
     }
     ap.sm_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
     ap.status = h->d_status;

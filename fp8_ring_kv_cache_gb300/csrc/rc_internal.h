@@ -82,6 +82,9 @@ struct AttnParams {
     // 128) is occupied by one write group, so one K and one V scale per head
     // cover the tile; tiles 0..255
     uint64_t uniform[4];
+    // tile j (not uniform) made of two write groups, slots [0, b) and [b, 128)
+    // of a full tile: split[j] = b (1..127), else 0
+    uint8_t split[256];
     float sm_log2;         // log2(e) / sqrt(D)
     int* status;           // device status word
 };

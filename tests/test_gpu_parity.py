@@ -102,6 +102,37 @@ def test_ragged_partial_ring(rc, D):
         pr.attend_check(layer, qq)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_tiles(rc, D):
+    # A full 8-tile ring written as runs whose ends fall at columns 1, 31, 32,
+    # 33, 64, 96 and 127 of tiles 0..6 (two write groups per tile), with tile 7
+    # holding three groups; neighbouring runs differ 8x in K and 4x in V
+    # magnitude, so the two groups of a tile carry different scales.  Then a
+    # write that wraps onto slots 0..199 (tile 1 split at column 72) and a
+    # delta rotation.
+    H, C = 4, 1024
+    cuts = [0, 1, 128 + 31, 256 + 32, 384 + 33, 512 + 64, 640 + 96, 768 + 127, 896 + 10, 896 + 70, 1024]
+    pr = Pair(rc, 1, H, D, C, max_write=C)
+    for i in range(len(cuts) - 1):
+        n = cuts[i + 1] - cuts[i]
+        ks, vs = (0.25, 0.5) if i % 2 == 0 else (2.0, 2.0)
+        k = si.normal_bf16(n, H, D, 900 + i, "cuda", torch.full((H, 1), ks))
+        v = si.normal_bf16(n, H, D, 950 + i, "cuda", torch.full((H, 1), vs))
+        pr.write(0, k, v, np.arange(cuts[i], cuts[i + 1]))
+    pr.check(0, "split runs")
+    n_last = cuts[-1] - cuts[-2]
+    pr.attend_check(0, si.normal_bf16(n_last, H, D, 990, "cuda"))
+    k = si.normal_bf16(200, H, D, 991, "cuda", torch.full((H, 1), 4.0))
+    v = si.normal_bf16(200, H, D, 992, "cuda")
+    pr.write(0, k, v, np.arange(C, C + 200))
+    pr.check(0, "wrapped write")
+    q = si.normal_bf16(200, H, D, 993, "cuda")
+    pr.attend_check(0, q)
+    pr.delta(-C)
+    pr.check(0, "after delta")
+    pr.attend_check(0, q)
+
+
 def test_production_call(rc):
     t = si.production_tensors(11, "cuda")
     C = si.PROD_SLOTS
