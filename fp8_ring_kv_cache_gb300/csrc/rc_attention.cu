@@ -109,6 +109,51 @@ __device__ __forceinline__ void e4m3x4_to_f16x4_div256(uint32_t w, uint32_t& lo,
     hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
 }
 
+// Softmax of the ring's last tile (fewer than 128 slots) when one write group
+// fills it: the uniform arithmetic with the columns past the ring's end cut to
+// -inf.  Once a call, so it is kept out of line.  Returns (new running max,
+// rescale factor of the old one, the tile's row sum of P'); P goes to TMEM
+// columns 0..63.
+__device__ __noinline__ float3 last_tile_softmax(uint32_t s_tm, int nvalid, float cu, float lsv0, float lsv,
+                                                 float m_run) {
+    uint32_t v[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32_async(s_tm + 32 * c, v[c]);
+    tmem_wait_ld_dep(v[0]);
+    reg_fence(v[1]);
+    reg_fence(v[2]);
+    reg_fence(v[3]);
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (32 * c + k >= nvalid) v[c][k] = __float_as_uint(-INFINITY);
+            mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[c][k]));
+        }
+    const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cu;
+    const bool bump = (m_run == -INFINITY) || (m_tile > m_run + 8.f);
+    const float m_new = bump ? fmaxf(m_run, m_tile) : m_run;
+    const float m_fin = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = bump ? ex2(m_run - m_fin) : 1.f;
+    const float nmu = lsv0 - (m_fin + lsv);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+            const float q0 = ex2(fmaf(__uint_as_float(v[c][k]), cu, nmu));
+            const float q1 = ex2(fmaf(__uint_as_float(v[c][k + 1]), cu, nmu));
+            sum += q0 + q1;
+            __half2 h = __floats2half2_rn(q0, q1);
+            pk[k / 2] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        tmem_st16(s_tm + 16 * c, pk);
+    }
+    return make_float3(m_new, alpha, sum);
+}
+
 // Softmax of any other tile (per-column scales, and on a masked tile or one
 // the ring ends inside, a validity test): pass A and pass B each read the
 // scores from TMEM in 32-column chunks.  Rare on a full ring, so it is kept
@@ -498,7 +543,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             // pass B (the probabilities) both run from the registers.  The ring's
             // last tile (fewer than 128 slots) takes its own instance, so the
             // column cut costs the full tiles nothing.
-            auto uniform_tile = [&](auto partial) {
+            auto uniform_tile = [&]() {
                     uint32_t v0[32], v1[32], v2[32], v3[32];
                     tmem_ld32_async(s_tm, v0);
                     tmem_ld32_async(s_tm + 32, v1);
@@ -508,18 +553,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     reg_fence(v1);
                     reg_fence(v2);
                     reg_fence(v3);
-                    if constexpr (decltype(partial)::value) {
-                        // the ring's last tile: columns past its end score -inf
-                        auto cut = [&](uint32_t (&v)[32], int c) {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                if (32 * c + k >= nvalid) v[k] = __float_as_uint(-INFINITY);
-                        };
-                        cut(v0, 0);
-                        cut(v1, 1);
-                        cut(v2, 2);
-                        cut(v3, 3);
-                    }
                     auto chunk_max = [](const uint32_t (&v)[32]) {
                         float t[11];
 #pragma unroll
@@ -666,9 +699,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             };
             const int sb = uni ? 0 : static_cast<int>(p.split[j]);
             if (__builtin_expect(uni && nvalid == kTileSlots, 1)) {
-                uniform_tile(std::false_type{});
+                uniform_tile();
             } else if (uni) {
-                uniform_tile(std::true_type{});
+                const float3 r = last_tile_softmax(s_tm, nvalid, cu, lsv0, lsv, m_run);
+                m_new = r.x;
+                alpha = r.y;
+                ls[0].x = r.z;
             } else if (sb != 0) {
                 split_tile(sb);
             } else {
