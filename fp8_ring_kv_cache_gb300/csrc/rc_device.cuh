@@ -319,6 +319,18 @@ __device__ __forceinline__ uint32_t map_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void dsmem_max_u32(uint32_t addr, uint32_t v) {
     asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Split cluster barrier: arrive (no ordering) now, wait later.  Waiting on an
+// arrival made at kernel start guarantees every CTA of the cluster is running,
+// which a CTA needs before it touches another's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");

@@ -7,7 +7,8 @@
 // K2 write_kernel: one thread-block cluster of 8 CTAs per head.  Each CTA
 //    copies its share of the n tokens (one bf16 K row and V row per token)
 //    into shared memory, rotates K, and reduces the head's amax for
-//    K and for V across the cluster through distributed shared memory; then
+//    K and for V across the cluster (each CTA pushes its partial maxima into
+//    every CTA's shared table; one cluster barrier); then
 //    every element becomes the E4M3 code of fl32(x / s) with
 //    s = fl32(amax / 448) and is scattered into its ring slot: K rows into the
 //    swizzled K tile, V through a shared-memory transpose into the Vt tile.
@@ -65,8 +66,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     uint8_t* vstage = smem + S::kStage;
     int32_t* sslot = reinterpret_cast<int32_t*>(smem + S::kSlot);
     __shared__ float red[2][kWriteWarps];
-    __shared__ float cta_amax[2];
-    __shared__ float scales[2];
+    __shared__ float amax_tab[2][kWriteCluster];  // [K / V][cluster rank]: each CTA's partial amax
 
     const int h = blockIdx.y;
     const int crank = blockIdx.x;     // the cluster spans blockIdx.x
@@ -76,6 +76,8 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     const int t1 = min(p.n, t0 + tpc);
     const int nbatch = (t1 - t0 + kWriteTB - 1) / kWriteTB;
     const int dim0 = lane * EPL;
+    // every CTA of the cluster is running once this barrier phase completes
+    cluster_arrive_relaxed();
 
     // slot of token t: floormod(pos - delta_total, C); an arithmetic run starts at slot0
     auto slot_of = [&](int t) -> int {
@@ -141,6 +143,8 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         {
 #pragma unroll
             for (int i = 0; i < kWritePer; ++i) {
+                // past the batch's end a warp repeats its last token, which the max
+                // already holds: no branch, so the tokens' work can overlap
                 const int tl = warp + kWriteWarps * i;
                 if (tl >= cnt) break;
                 float k[EPL], v[EPL];
@@ -150,7 +154,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
                     amk = fmaxf(amk, fabsf(k[e]));
                     amv = fmaxf(amv, fabsf(v[e]));
                 }
-                if (p.kraw != nullptr) {
+                if (p.kraw != nullptr && warp + kWriteWarps * i < cnt) {
                     // read-time ablation store: the unrotated bf16 row and its angles
                     const int slot = slot_of(tb + tl);
                     const size_t dst = (static_cast<size_t>(h) * p.Cpad + slot) * D + dim0;
@@ -180,54 +184,73 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         red[1][warp] = amv;
     }
     __syncthreads();
-    if (threadIdx.x < 2) {
+    // ---- across the cluster: each CTA pushes its two maxima into every CTA's
+    // table, one barrier makes them visible, and every thread reads its own table
+    // phase 2's first angles are on their way while the cluster agrees on the scales
+    float2 cs[kWritePer][EPL / 2];
+    if (nbatch > 0) fetch_rope(t0, min(kWriteTB, t1 - t0), cs);
+    cluster_wait();  // (the arrival at kernel start) every CTA is running
+    if (threadIdx.x < 2 * kWriteCluster) {
+        const int which = threadIdx.x / kWriteCluster, r = threadIdx.x % kWriteCluster;
         float m = 0.f;
-        for (int w = 0; w < kWriteWarps; ++w) m = fmaxf(m, red[threadIdx.x][w]);
-        cta_amax[threadIdx.x] = m;
+        for (int w = 0; w < kWriteWarps; ++w) m = fmaxf(m, red[which][w]);
+        dsmem_st_u32(map_shared(&amax_tab[which][crank], r), __float_as_uint(m));
     }
-    // ---- across the cluster: every CTA reads the 8 partial maxima
-    cluster_sync();
-    if (threadIdx.x < 2) {
-        float m = 0.f;
-        for (uint32_t r = 0; r < kWriteCluster; ++r)
-            m = fmaxf(m, __uint_as_float(dsmem_ld_u32(map_shared(&cta_amax[threadIdx.x], r))));
-        scales[threadIdx.x] = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
+    cluster_sync();  // the pushes are visible; no CTA touches another's shared memory after this
+    float mk = 0.f, mv = 0.f;
+#pragma unroll
+    for (int r = 0; r < kWriteCluster; ++r) {
+        mk = fmaxf(mk, amax_tab[0][r]);
+        mv = fmaxf(mv, amax_tab[1][r]);
     }
-    cluster_sync();  // no CTA touches another's shared memory after this point
-    const float sK = scales[0], sV = scales[1];
+    const float sK = (mk > 0.f) ? __fdiv_rn(mk, 448.f) : 1.f;
+    const float sV = (mv > 0.f) ? __fdiv_rn(mv, 448.f) : 1.f;
     const float rK = __frcp_rn(sK), rV = __frcp_rn(sV);
+    // fl32(x / s) by div_by_scale's three steps on packed pairs (fma(q0, -s, x)
+    // equals fma(-q0, s, x) exactly)
+    const float2 rK2 = make_float2(rK, rK), nsK2 = make_float2(-sK, -sK);
+    const float2 rV2 = make_float2(rV, rV), nsV2 = make_float2(-sV, -sV);
+    auto div2 = [](float2 x, float2 r, float2 ns) {
+        const float2 q0 = mul2(x, r);
+        return fma2(fma2(q0, ns, x), r, q0);
+    };
 
     // ---- phase 2: quantise and scatter (a single batch is still staged)
     for (int b = 0; b < nbatch; ++b) {
         const int tb = t0 + b * kWriteTB;
         const int cnt = min(kWriteTB, t1 - tb);
-        float2 cs[kWritePer][EPL / 2];
-        fetch_rope(tb, cnt, cs);
+        if (b > 0) fetch_rope(tb, cnt, cs);
         if (nbatch > 1) stage_batch(tb, cnt);
 #pragma unroll
         for (int i = 0; i < kWritePer; ++i) {
-            const int tl = warp + kWriteWarps * i;
+            // past the batch's end a warp repeats its last token's stores (same
+            // values to the same places) into staging rows nobody reads
+            const int tw = warp + kWriteWarps * i, tl = tw;
             if (tl >= cnt) break;
             float k[EPL], v[EPL];
             row(tl, cs[i], k, v);
             const int slot = slot_of(tb + tl);
-            if (lane == 0) sslot[tl] = slot;
+            if (lane == 0) sslot[tw] = slot;
             uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
             float qk[EPL], qv[EPL];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                qk[e] = div_by_scale(k[e], sK, rK);
-                qv[e] = div_by_scale(v[e], sV, rV);
+            for (int e = 0; e < EPL; e += 2) {
+                const float2 a = div2(make_float2(k[e], k[e + 1]), rK2, nsK2);
+                const float2 b = div2(make_float2(v[e], v[e + 1]), rV2, nsV2);
+                qk[e] = a.x;
+                qk[e + 1] = a.y;
+                qv[e] = b.x;
+                qv[e + 1] = b.y;
             }
             if constexpr (EPL == 4) {
                 *reinterpret_cast<uint32_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
                     e4m3x2(qk[0], qk[1]) | (e4m3x2(qk[2], qk[3]) << 16);
-                *reinterpret_cast<uint32_t*>(vstage + tl * S::kVRow + dim0) =
+                *reinterpret_cast<uint32_t*>(vstage + tw * S::kVRow + dim0) =
                     e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             } else {
                 *reinterpret_cast<uint16_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
                     static_cast<uint16_t>(e4m3x2(qk[0], qk[1]));
-                *reinterpret_cast<uint16_t*>(vstage + tl * S::kVRow + dim0) =
+                *reinterpret_cast<uint16_t*>(vstage + tw * S::kVRow + dim0) =
                     static_cast<uint16_t>(e4m3x2(qv[0], qv[1]));
             }
             if (lane == 0) {
