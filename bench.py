@@ -45,8 +45,8 @@ TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
     # the production call (ncu, profiles/attn_kernel_production_call.md), valid
     # while rc_attention.cu has this hash
-    "attention": {"bytes": 87.18e6,
-                  "src_sha256": "f529c6f77c96889c49f190dbd062bfb510ffffa41f381c10ab1c5d146eed3f81"},
+    "attention": {"bytes": 87.54e6,
+                  "src_sha256": "dff29bc3193b23431ee739c502109a235ee9cea4afd9c66da51d77ea8881250a"},
 }
 
 
