@@ -69,15 +69,20 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
+        self.sink = None
 
     def start(self):
+        import tempfile
+        # samples go to a file, not a pipe: a long run would fill a pipe and stall the sampler
+        self.sink = tempfile.TemporaryFile(mode="w+")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=self.sink, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
@@ -85,7 +90,10 @@ class ClockSampler:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        self.proc.wait(timeout=10)
+        self.sink.seek(0)
+        out = self.sink.read()
+        self.sink.close()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -293,6 +301,93 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(calls=args.cpu_calls)
     return res
+
+
+def run_sustained(args) -> dict:
+    """Sustained workload: `--sustained N` chunks of 240 calls at the production
+    shape with a per-head standard deviation drawn once per (layer, head) from
+    U[0.5, 4] for Q, K and V alike (the 240 distinct inputs of a chunk are
+    generated once and reused).  Each chunk writes 757 new positions (4 passes
+    rewrite them) and the window restarts every 300 chunks: one delta rotation
+    of every layer by -(oldest stored position).  Per-chunk times come from
+    events on the launching stream; the steady state leaves out the first
+    three chunks (the ring fills during the first)."""
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+    import synth_inputs as si
+
+    dev = torch.device("cuda", 0)
+    seed = 41
+    std = si.head_std(L, H, seed)
+    cache = rc.RingKVCache(L, H, D, C, max_write=C)
+    K = torch.empty(PASSES, L, N_NEW, H, D, dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    Q = torch.empty_like(K)
+    for pas in range(PASSES):
+        for layer in range(L):
+            k, v, q = si.chunk_tensors(seed, 0, pas, layer, dev, std=std[layer])
+            K[pas, layer], V[pas, layer], Q[pas, layer] = k, v, q
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    for layer in range(L):
+        sl = std[layer].view(H, 1)
+        kp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, layer, 7), dev, sl)
+        vp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, layer, 8), dev, sl)
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+    stream = torch.cuda.current_stream()
+    newest = PREFILL - 1
+    nch, every = args.sustained, 300
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nch)]
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nch // every)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0, period_ms=500)
+    clocks.start()
+    launches0 = cache.launch_count
+    t0 = time.perf_counter()
+    for c in range(nch):
+        pos = np.arange(newest + 1, newest + 1 + N_NEW)
+        ev[c][0].record(stream)
+        for pas in range(PASSES):
+            for layer in range(L):
+                cache.write(layer, K[pas, layer], V[pas, layer], pos)
+                cache.attend(layer, Q[pas, layer], out)
+        ev[c][1].record(stream)
+        newest += N_NEW
+        if (c + 1) % every == 0:
+            oldest = newest - C + 1          # the ring is full after the first chunk
+            r = rev[(c + 1) // every - 1]
+            r[0].record(stream)
+            cache.delta_rotate(-oldest)
+            r[1].record(stream)
+            newest -= oldest
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t0
+    clk = clocks.stop()
+    cache.sync()
+    launches = cache.launch_count - launches0
+    ms = sorted(a.elapsed_time(b) for a, b in ev[3:])
+    resets = [a.elapsed_time(b) for a, b in rev]
+    mean = statistics.mean(ms)
+    return {
+        "mode": "sustained",
+        "metric": "ms per 240-call chunk, steady state (mean, p50, p99, max)",
+        "chunks": nch, "steady_chunks": len(ms),
+        "ms_per_chunk_mean": round(mean, 4),
+        "ms_per_chunk_p50": round(ms[len(ms) // 2], 4),
+        "ms_per_chunk_p99": round(ms[min(len(ms) - 1, int(0.99 * len(ms)))], 4),
+        "ms_per_chunk_max": round(ms[-1], 4),
+        "calls_per_s": round(CALLS_PER_CHUNK / mean * 1e3, 2),
+        "resets": len(resets), "ms_per_reset_mean": round(statistics.mean(resets), 4) if resets else None,
+        "wall_s": round(wall_s, 2), "gpu_launches": int(launches),
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "sustained chunks: 4 passes x 60 layers x (write 757 new tokens + attention of 757 "
+                               "queries over 5,788 FP8 slots), 48 heads x 128, per-head std U[0.5, 4] for Q, K, V; "
+                               "window restart (delta = -oldest position) every 300 chunks",
+                   "layers": L, "heads": H, "head_dim": D, "slots": C, "new_tokens": N_NEW, "prefill": PREFILL},
+        "clocks": clk,
+    }
 
 
 def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
@@ -517,9 +612,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-calls", type=int, default=3, help="oracle calls timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained", type=int, default=0, metavar="CHUNKS",
+                    help="run the sustained workload for CHUNKS chunks (e.g. 3600) and exit")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args.profile)
+        return
+    if args.sustained:
+        print(json.dumps(run_sustained(args)), flush=True)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
