@@ -390,6 +390,74 @@ def run_sustained(args) -> dict:
     }
 
 
+def run_stress(args) -> dict:
+    """Reset stress at 60 layers: every ring full at positions up to 200,000, then
+    `--stress N` steps of (delta rotation of all layers by a delta drawn from
+    U_int[-200000, 0], then write 757 tokens at the next positions and attend,
+    in every layer).  Events time the rotation and the 60 write + attend pairs
+    of each step separately."""
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+    import synth_inputs as si
+
+    dev = torch.device("cuda", 0)
+    seed = 31
+    cache = rc.RingKVCache(L, H, D, C, max_write=C)
+    top = 200_000
+    k0 = si.normal_bf16(C, H, D, si.subseed(seed, 1), dev)
+    v0 = si.normal_bf16(C, H, D, si.subseed(seed, 2), dev)
+    for layer in range(L):
+        cache.write(layer, k0, v0, np.arange(top - C + 1, top + 1))
+    K = torch.empty(L, N_NEW, H, D, dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    Q = torch.empty_like(K)
+    for layer in range(L):
+        K[layer] = si.normal_bf16(N_NEW, H, D, si.subseed(seed, 10, layer, 1), dev)
+        V[layer] = si.normal_bf16(N_NEW, H, D, si.subseed(seed, 10, layer, 2), dev)
+        Q[layer] = si.normal_bf16(N_NEW, H, D, si.subseed(seed, 10, layer, 3), dev)
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    deltas = si.stress_deltas(seed, args.stress)
+    stream = torch.cuda.current_stream()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+    rot, calls = [mk() for _ in deltas], [mk() for _ in deltas]
+    nxt = top + 1
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0, period_ms=200)
+    clocks.start()
+    for i, d in enumerate(deltas):
+        rot[i][0].record(stream)
+        cache.delta_rotate(d)
+        rot[i][1].record(stream)
+        nxt += d
+        pos = np.arange(nxt, nxt + N_NEW)
+        nxt += N_NEW
+        calls[i][0].record(stream)
+        for layer in range(L):
+            cache.write(layer, K[layer], V[layer], pos)
+            cache.attend(layer, Q[layer], out)
+        calls[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    cache.sync()
+    r = [a.elapsed_time(b) for a, b in rot]
+    c = [a.elapsed_time(b) for a, b in calls]
+    return {
+        "mode": "stress",
+        "metric": "ms per delta rotation of 60 layers and per 60 (write + attend) calls after it",
+        "steps": len(deltas), "delta_range": [min(deltas), max(deltas)],
+        "ms_per_rotation_mean": round(statistics.mean(r), 4), "ms_per_rotation_max": round(max(r), 4),
+        "rotation_gbs": round(ROTATE_BYTES / (statistics.mean(r) * 1e-3) / 1e9, 1),
+        "ms_per_60_calls_mean": round(statistics.mean(c), 4), "ms_per_60_calls_max": round(max(c), 4),
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "reset stress: full 5,788-slot rings at positions up to 200,000 in 60 layers, "
+                               "then delta ~ U_int[-200000, 0] + write 757 + attend in every layer, per step",
+                   "layers": L, "heads": H, "head_dim": D, "slots": C, "new_tokens": N_NEW},
+        "clocks": clk,
+    }
+
+
 def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
     import numpy as np
     import torch
@@ -614,12 +682,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sustained", type=int, default=0, metavar="CHUNKS",
                     help="run the sustained workload for CHUNKS chunks (e.g. 3600) and exit")
+    ap.add_argument("--stress", type=int, default=0, metavar="STEPS",
+                    help="run the reset stress at 60 layers for STEPS steps (e.g. 100) and exit")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args.profile)
         return
     if args.sustained:
         print(json.dumps(run_sustained(args)), flush=True)
+        return
+    if args.stress:
+        print(json.dumps(run_stress(args)), flush=True)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
