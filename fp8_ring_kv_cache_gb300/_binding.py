@@ -65,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_occupancy": ([P, I], I),
         "rc_cache_delta_total": ([P], I64),
         "rc_cache_launch_count": ([P], I64),
+        "rc_tile_kinds": ([P, I, P, P], I),
         "rc_ring_write_noalloc": ([ctypes.POINTER(rc_ring_view), P, P, P, I, I64, ctypes.c_int32,
                                    ctypes.c_double, P], I),
     }
@@ -183,6 +184,15 @@ def rc_cache_export_readtime(h, heads: int, head_dim: int, slots: int) -> dict:
     _check(lib.rc_cache_export_readtime(h, *[_np_ptr(st[k]) for k in ("kcodes", "kscale", "vcodes", "vscale")]),
            "rc_cache_export_readtime")
     return st
+
+
+def rc_tile_kinds(grp) -> tuple[np.ndarray, np.ndarray]:
+    """(uniform [4] uint64 bitmask, split [256] uint8) of a ring's slot groups."""
+    g = np.ascontiguousarray(np.asarray(grp, dtype=np.int32))
+    uniform = np.zeros(4, np.uint64)
+    split = np.zeros(256, np.uint8)
+    _check(lib.rc_tile_kinds(_np_ptr(g), int(g.shape[0]), _np_ptr(uniform), _np_ptr(split)), "rc_tile_kinds")
+    return uniform, split
 
 
 def rc_cache_occupancy(h, layer: int) -> int:

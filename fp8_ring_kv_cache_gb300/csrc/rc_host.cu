@@ -120,17 +120,15 @@ void free_all(rc_cache* h) {
 
 // Tiles whose slots are all occupied by a single write group (uniform), and
 // full tiles made of two runs, slots [0, b) of one write group and [b, 128) of
-// another (split[t] = b, 1..127; 0 for every other tile).
-void refresh_uniform(rc_cache* h, int layer) {
-    if (!h->uniform_dirty[layer]) return;
-    auto& m = h->uniform[layer];
-    auto& sp = h->split[layer];
+// another (split[t] = b, 1..127; 0 for every other tile).  g: the layer's
+// group per slot (-1 empty), C slots; tiles past 256 are left unmarked.
+void classify_tiles(const int32_t* g, int C, std::array<uint64_t, 4>& m, std::array<uint8_t, 256>& sp) {
     m = {0, 0, 0, 0};
     sp.fill(0);
-    const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
-    for (int t = 0; t < h->T && t < 256; ++t) {
+    const int T = (C + kTileSlots - 1) / kTileSlots;
+    for (int t = 0; t < T && t < 256; ++t) {
         // the ring's slots of the tile (the last tile may end before 128)
-        const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, h->C);
+        const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, C);
         if (g[s0] < 0) continue;
         int b = s0 + 1;
         while (b < s1 && g[b] == g[s0]) ++b;
@@ -143,6 +141,11 @@ void refresh_uniform(rc_cache* h, int layer) {
         while (e < s1 && g[e] == g[b]) ++e;
         if (e == s1) sp[t] = static_cast<uint8_t>(b - s0);
     }
+}
+
+void refresh_uniform(rc_cache* h, int layer) {
+    if (!h->uniform_dirty[layer]) return;
+    classify_tiles(h->grp.data() + static_cast<size_t>(layer) * h->C, h->C, h->uniform[layer], h->split[layer]);
     h->uniform_dirty[layer] = 0;
 }
 
@@ -659,5 +662,15 @@ int rc_cache_occupancy(const rc_cache* h, int layer) {
 int64_t rc_cache_delta_total(const rc_cache* h) { return h ? h->delta_total : 0; }
 
 int64_t rc_cache_launch_count(const rc_cache* h) { return h ? h->launches : 0; }
+
+int rc_tile_kinds(const int32_t* grp, int slots, uint64_t* uniform, uint8_t* split) {
+    if (!grp || !uniform || !split || slots < 1 || slots > 32768) return RC_ERR_ARG;
+    std::array<uint64_t, 4> m;
+    std::array<uint8_t, 256> sp;
+    classify_tiles(grp, slots, m, sp);
+    std::memcpy(uniform, m.data(), sizeof(m));
+    std::memcpy(split, sp.data(), sizeof(sp));
+    return RC_OK;
+}
 
 }  // extern "C"

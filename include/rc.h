@@ -237,6 +237,21 @@ int64_t rc_cache_delta_total(const rc_cache *h);
 /* Number of kernel launches this handle has made (for launch accounting). */
 int64_t rc_cache_launch_count(const rc_cache *h);
 
+/*
+ * How the attention call treats the KV tiles of one ring (host only: no
+ * device, no handle).  grp[0 .. slots) is the ring's write group per slot
+ * (-1 = empty); tile t covers slots [128 t, min(128 t + 128, slots)).
+ *   uniform[t / 64] bit t % 64: every slot of tile t holds the same write
+ *     group, so one K and one V scale per head cover it (the fast path);
+ *   split[t] = b in 1..127: tile t has 128 slots, [128 t, 128 t + b) hold one
+ *     write group and [128 t + b, 128 t + 128) another (where a write's run of
+ *     slots ends inside the tile; the two-run path); otherwise 0.
+ * Every other tile takes the general path (per-slot scales and validity).
+ * uniform (4 words) and split (256 bytes) are caller-owned host memory.
+ * Errors: RC_ERR_ARG if a pointer is NULL or slots is outside 1 .. 32768.
+ */
+int rc_tile_kinds(const int32_t *grp, int slots, uint64_t *uniform, uint8_t *split);
+
 #ifdef __cplusplus
 }
 #endif
