@@ -12,6 +12,9 @@ The rings (4.3 GB) and the 240 distinct (K, V, Q) inputs of a chunk (6.7 GB)
 are far larger than L2, so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --sustained 3600    # per-head std U[0.5, 4], restart every 300 chunks: mean / p99 ms per chunk
+  python bench.py --stress 100        # 60 full rings, 100 deltas ~ U_int[-200000, 0], each + write + attend
+  python bench.py --profile attention|write|rotate   # small fixed cases for ncu captures
 
 Under torchrun (N > 1) every rank runs its own session on its own GPU (the
 method is batch-1 per session; replicas, weak scaling) and rank 0 prints the
