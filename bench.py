@@ -14,6 +14,7 @@ are far larger than L2, so no L2 flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --sustained 3600    # per-head std U[0.5, 4], restart every 300 chunks: mean / p99 ms per chunk
   python bench.py --stress 100        # 60 full rings, 100 deltas ~ U_int[-200000, 0], each + write + attend
+  python bench.py --copy-window       # the copy-based window (shift every chunk) against the ring
   python bench.py --profile attention|write|rotate   # small fixed cases for ncu captures
 
 Under torchrun (N > 1) every rank runs its own session on its own GPU (the
@@ -461,6 +462,95 @@ def run_stress(args) -> dict:
     }
 
 
+def run_copy_window(args) -> dict:
+    """The copy-based window against the ring on the chunk workload.  A step is
+    the chunk (240 calls) and the 60-layer delta rotation that restarts the
+    window, as in the default bench; the copy-based cache also moves every
+    stored token 757 slots down in every layer before the chunk
+    (rc_cache_window_shift), as a cache that concatenates must.  Same inputs,
+    one cache at a time; per-part times from events on the launching stream."""
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+    import synth_inputs as si
+
+    dev = torch.device("cuda", 0)
+    seed = 21
+    mult = si.outlier_mask(H, D, seed)
+    K = torch.empty(PASSES, L, N_NEW, H, D, dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    Q = torch.empty_like(K)
+    for pas in range(PASSES):
+        for layer in range(L):
+            k, v, q = si.chunk_tensors(seed, 0, pas, layer, dev, mult=mult)
+            K[pas, layer], V[pas, layer], Q[pas, layer] = k, v, q
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    kp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, 7), dev, mult)
+    vp = si.normal_bf16(PREFILL, H, D, si.subseed(seed, 8), dev, mult)
+    chunk_pos = np.arange(PREFILL, PREFILL + N_NEW)
+    stream = torch.cuda.current_stream()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+    res = {}
+    for variant in ("ring", "copy"):
+        cache = rc.RingKVCache(L, H, D, C, max_write=C, copy_window=(variant == "copy"))
+        for layer in range(L):
+            cache.write(layer, kp, vp, np.arange(0, PREFILL))
+
+        def step(ev=None):
+            if ev is not None:
+                ev[0][0].record(stream)
+            if variant == "copy":
+                cache.window_shift(N_NEW)
+            if ev is not None:
+                ev[0][1].record(stream)
+                ev[1][0].record(stream)
+            for pas in range(PASSES):
+                for layer in range(L):
+                    cache.write(layer, K[pas, layer], V[pas, layer], chunk_pos)
+                    cache.attend(layer, Q[pas, layer], out)
+            if ev is not None:
+                ev[1][1].record(stream)
+                ev[2][0].record(stream)
+            cache.delta_rotate(-N_NEW)
+            if ev is not None:
+                ev[2][1].record(stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [[mk(), mk(), mk()] for _ in range(args.steps)]
+        t0, t1 = mk()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        cache.sync()
+        part = lambda j: statistics.mean(e[j][0].elapsed_time(e[j][1]) for e in evs)  # noqa: E731
+        res[variant] = {"ms_per_step": round(t0.elapsed_time(t1) / args.steps, 4),
+                        "ms_shift": round(part(0), 4), "ms_chunk": round(part(1), 4),
+                        "ms_delta": round(part(2), 4)}
+        cache.close()
+        del cache
+    shift_bytes = 2.0 * 2 * L * H * C * D + 2.0 * 2 * L * H * C * 4   # codes and scales, read + written
+    ms = res["copy"]["ms_shift"]
+    return {
+        "mode": "copy_window",
+        "metric": "ms per step (chunk + window restart), ring vs copy-based window",
+        "steps": args.steps, "warmup": args.warmup,
+        "ring": res["ring"], "copy": res["copy"],
+        "copy_extra_ms_per_step": round(res["copy"]["ms_per_step"] - res["ring"]["ms_per_step"], 4),
+        "shift_gbs": round(shift_bytes / (ms * 1e-3) / 1e9, 1) if ms > 0 else None,
+        "shift_bytes": shift_bytes,
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "chunk of 240 calls (4 passes x 60 layers x (write 757 + attention of 757 queries "
+                               "over 5,788 FP8 slots), 48 heads x 128) + 60-layer delta rotation; the copy-based "
+                               "cache also shifts every layer's slots by 757 before each chunk",
+                   "layers": L, "heads": H, "head_dim": D, "slots": C, "new_tokens": N_NEW, "prefill": PREFILL},
+    }
+
+
 def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
     import numpy as np
     import torch
@@ -687,6 +777,8 @@ def main():
                     help="run the sustained workload for CHUNKS chunks (e.g. 3600) and exit")
     ap.add_argument("--stress", type=int, default=0, metavar="STEPS",
                     help="run the reset stress at 60 layers for STEPS steps (e.g. 100) and exit")
+    ap.add_argument("--copy-window", action="store_true",
+                    help="time the copy-based window against the ring on the chunk workload and exit")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args.profile)
@@ -696,6 +788,9 @@ def main():
         return
     if args.stress:
         print(json.dumps(run_stress(args)), flush=True)
+        return
+    if args.copy_window:
+        print(json.dumps(run_copy_window(args)), flush=True)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

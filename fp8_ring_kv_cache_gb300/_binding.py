@@ -24,6 +24,7 @@ RC_ERR_OOM = -4
 RC_ERR_TIMEOUT = -5
 RC_ERR_UNSUPPORTED = -6
 RC_F_READTIME_ABLATION = 1
+RC_F_COPY_WINDOW = 2
 EMPTY = np.iinfo(np.int64).min
 
 
@@ -55,6 +56,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_create": ([ctypes.POINTER(rc_config), I, ctypes.POINTER(P)], I),
         "rc_cache_write": ([P, I, P, P, P, I, P], I),
         "rc_cache_delta_rotate": ([P, I64, P], I),
+        "rc_cache_window_shift": ([P, I64, P], I),
         "rc_attend": ([P, I, P, P, I, P], I),
         "rc_attend_readtime": ([P, I, P, P, I, P], I),
         "rc_cache_destroy": ([P], None),
@@ -144,6 +146,10 @@ def rc_cache_delta_rotate(h, delta: int, stream=None) -> None:
     _check(lib.rc_cache_delta_rotate(h, int(delta), _stream_ptr(stream)), "rc_cache_delta_rotate")
 
 
+def rc_cache_window_shift(h, k: int, stream=None) -> None:
+    _check(lib.rc_cache_window_shift(h, int(k), _stream_ptr(stream)), "rc_cache_window_shift")
+
+
 def rc_attend(h, layer: int, Q, out, heads: int, head_dim: int, stream=None) -> None:
     import torch
     n = int(Q.shape[0])
@@ -214,10 +220,11 @@ class RingKVCache:
     """Owns one rc_cache handle; methods forward to the C entry points."""
 
     def __init__(self, layers: int, heads: int, head_dim: int, slots: int, max_write: int | None = None,
-                 rope_base: float = 10000.0, readtime_ablation: bool = False, device: int = 0):
+                 rope_base: float = 10000.0, readtime_ablation: bool = False, device: int = 0,
+                 copy_window: bool = False):
         self.layers, self.heads, self.head_dim, self.slots = layers, heads, head_dim, slots
         self.max_write = slots if max_write is None else max_write
-        flags = RC_F_READTIME_ABLATION if readtime_ablation else 0
+        flags = (RC_F_READTIME_ABLATION if readtime_ablation else 0) | (RC_F_COPY_WINDOW if copy_window else 0)
         self.handle = rc_cache_create(layers, heads, head_dim, slots, self.max_write, rope_base, flags, device)
 
     def close(self) -> None:
@@ -233,6 +240,9 @@ class RingKVCache:
 
     def delta_rotate(self, delta, stream=None):
         rc_cache_delta_rotate(self.handle, delta, stream)
+
+    def window_shift(self, k, stream=None):
+        rc_cache_window_shift(self.handle, k, stream)
 
     def attend(self, layer, Q, out, stream=None):
         rc_attend(self.handle, layer, Q, out, self.heads, self.head_dim, stream)

@@ -7,6 +7,7 @@
 // at position p lives in slot floormod(p - delta_total, C).  A delta rotation
 // adds delta to every stored position and to delta_total, so no token moves.
 #include <algorithm>
+#include <utility>
 #include <array>
 #include <cmath>
 #include <cstdio>
@@ -46,6 +47,7 @@ struct rc_cache {
     int device = 0;
     int L = 0, H = 0, D = 0, C = 0, T = 0, Cpad = 0, max_write = 0;
     bool ablation = false;
+    bool copy_window = false;  // RC_F_COPY_WINDOW: a second bank for rc_cache_window_shift
     // device memory
     uint8_t* d_kc = nullptr;
     uint8_t* d_vt = nullptr;
@@ -61,6 +63,12 @@ struct rc_cache {
     uint8_t* d_rt_vt = nullptr;
     float* d_rt_sk = nullptr;
     float* d_rt_sv = nullptr;
+    // the copy-based window's second bank (same shapes as d_kc .. d_grp)
+    uint8_t* d2_kc = nullptr;
+    uint8_t* d2_vt = nullptr;
+    float* d2_sk = nullptr;
+    float* d2_sv = nullptr;
+    int32_t* d2_grp = nullptr;
     RopeEntry pool[kPoolEntries];
     uint64_t clock = 0;
     // host mirrors of the ring tables
@@ -77,6 +85,9 @@ struct rc_cache {
     uint32_t mark = 0;
     std::vector<double> theta;
     int64_t delta_total = 0, next_gid = 0, launches = 0;
+    // sum of the copy-based window's shifts: token at position p lives in
+    // slot floormod(p - delta_total - slot_shift, C) (0 for a plain ring)
+    int64_t slot_shift = 0;
     cudaStream_t last_stream = nullptr;
 };
 
@@ -109,6 +120,11 @@ void free_all(rc_cache* h) {
     cudaFree(h->d_rt_vt);
     cudaFree(h->d_rt_sk);
     cudaFree(h->d_rt_sv);
+    cudaFree(h->d2_kc);
+    cudaFree(h->d2_vt);
+    cudaFree(h->d2_sk);
+    cudaFree(h->d2_sv);
+    cudaFree(h->d2_grp);
     for (auto& e : h->pool) {
         cudaFree(e.d_table);
         cudaFree(e.d_pos);
@@ -257,6 +273,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
         return RC_ERR_ARG;
     if (cfg->head_dim != 64 && cfg->head_dim != 128) return RC_ERR_UNSUPPORTED;
     if (cfg->slots > 32768 || cfg->heads > 65535 || cfg->layers > 65535) return RC_ERR_UNSUPPORTED;
+    if ((cfg->flags & RC_F_READTIME_ABLATION) && (cfg->flags & RC_F_COPY_WINDOW)) return RC_ERR_UNSUPPORTED;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return RC_ERR_ARG;
     cudaDeviceProp prop{};
@@ -276,6 +293,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     h->Cpad = h->T * kTileSlots;
     h->max_write = cfg->max_write;
     h->ablation = (cfg->flags & RC_F_READTIME_ABLATION) != 0;
+    h->copy_window = (cfg->flags & RC_F_COPY_WINDOW) != 0;
 
     int st = RC_OK;
     const size_t rb = ring_bytes(h), sc = scale_count(h);
@@ -304,6 +322,13 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
         st |= dmalloc(&h->d_rt_sk, static_cast<size_t>(h->H) * h->Cpad);
         st |= dmalloc(&h->d_rt_sv, static_cast<size_t>(h->H) * h->Cpad);
     }
+    if (h->copy_window) {
+        st |= dmalloc(&h->d2_kc, rb);
+        st |= dmalloc(&h->d2_vt, rb);
+        st |= dmalloc(&h->d2_sk, sc);
+        st |= dmalloc(&h->d2_sv, sc);
+        st |= dmalloc(&h->d2_grp, static_cast<size_t>(h->L) * h->Cpad);
+    }
     if (st != RC_OK) {
         free_all(h);
         cudaGetLastError();  // clear the allocation error
@@ -314,6 +339,12 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
               cudaMemset(h->d_sv, 0, sizeof(float) * sc) == cudaSuccess &&
               cudaMemset(h->d_grp, 0xFF, sizeof(int32_t) * h->L * h->Cpad) == cudaSuccess &&
               cudaMemset(h->d_status, 0, sizeof(int)) == cudaSuccess;
+    if (ok && h->copy_window) {
+        ok = cudaMemset(h->d2_kc, 0, rb) == cudaSuccess && cudaMemset(h->d2_vt, 0, rb) == cudaSuccess &&
+             cudaMemset(h->d2_sk, 0, sizeof(float) * sc) == cudaSuccess &&
+             cudaMemset(h->d2_sv, 0, sizeof(float) * sc) == cudaSuccess &&
+             cudaMemset(h->d2_grp, 0xFF, sizeof(int32_t) * h->L * h->Cpad) == cudaSuccess;
+    }
     if (ok && h->ablation) {
         const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
         ok = cudaMemset(h->d_kraw, 0, raw * 2) == cudaSuccess && cudaMemset(h->d_vraw, 0, raw * 2) == cudaSuccess &&
@@ -375,7 +406,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
         h->mark = 1;
     }
     for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
         if (h->slot_mark[slot] == h->mark) return RC_ERR_ARG;
         h->slot_mark[slot] = h->mark;
     }
@@ -391,7 +422,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     auto& rc = h->refcnt[layer];
     auto& fl = h->freelist[layer];
     for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
         const int32_t old = h->grp[lb + slot];
         if (old >= 0) {
             if (--rc[old] == 0) fl.push_back(old);
@@ -403,7 +434,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     fl.pop_back();
     rc[g] = n;
     for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total, h->C);
+        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
         h->pos[lb + slot] = positions[t];
         h->gid[lb + slot] = h->next_gid;
         h->grp[lb + slot] = g;
@@ -422,8 +453,8 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     wp.rope = re.d_table;
     wp.pos = re.arith ? nullptr : re.d_pos;
     wp.p0 = positions[0];
-    wp.delta_total = h->delta_total;
-    wp.slot0 = static_cast<int>(floormod(positions[0] - h->delta_total, h->C));
+    wp.delta_total = h->delta_total + h->slot_shift;  // the kernel's slot mapping
+    wp.slot0 = static_cast<int>(floormod(positions[0] - h->delta_total - h->slot_shift, h->C));
     wp.status = h->d_status;
     wp.n = n;
     wp.H = h->H;
@@ -475,6 +506,54 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
         h->last_entry[l] = -1;
     }
     h->delta_total += delta;
+    h->last_stream = s;
+    return RC_OK;
+}
+
+int rc_cache_window_shift(rc_cache* h, int64_t k, void* stream) {
+    if (!h || k < 0) return RC_ERR_ARG;
+    if (!h->copy_window) return RC_ERR_STATE;
+    const int kk = static_cast<int>(k % h->C);
+    if (kk == 0) {
+        h->slot_shift += k;
+        return RC_OK;
+    }
+    if (check_sticky() != RC_OK) return RC_ERR_CUDA;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ShiftParams sp{};
+    sp.kc_src = h->d_kc;
+    sp.kc_dst = h->d2_kc;
+    sp.vt_src = h->d_vt;
+    sp.vt_dst = h->d2_vt;
+    sp.sk_src = h->d_sk;
+    sp.sk_dst = h->d2_sk;
+    sp.sv_src = h->d_sv;
+    sp.sv_dst = h->d2_sv;
+    sp.grp_src = h->d_grp;
+    sp.grp_dst = h->d2_grp;
+    sp.L = h->L;
+    sp.H = h->H;
+    sp.C = h->C;
+    sp.T = h->T;
+    sp.Cpad = h->Cpad;
+    sp.k = kk;
+    if (launch_window_shift(sp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    std::swap(h->d_kc, h->d2_kc);
+    std::swap(h->d_vt, h->d2_vt);
+    std::swap(h->d_sk, h->d2_sk);
+    std::swap(h->d_sv, h->d2_sv);
+    std::swap(h->d_grp, h->d2_grp);
+    // the host tables move the same way: slot s takes slot s + kk (mod C)
+    for (int l = 0; l < h->L; ++l) {
+        const size_t lb = static_cast<size_t>(l) * h->C;
+        std::rotate(h->pos.begin() + lb, h->pos.begin() + lb + kk, h->pos.begin() + lb + h->C);
+        std::rotate(h->gid.begin() + lb, h->gid.begin() + lb + kk, h->gid.begin() + lb + h->C);
+        std::rotate(h->grp.begin() + lb, h->grp.begin() + lb + kk, h->grp.begin() + lb + h->C);
+        h->uniform_dirty[l] = 1;
+    }
+    h->slot_shift += k;
     h->last_stream = s;
     return RC_OK;
 }

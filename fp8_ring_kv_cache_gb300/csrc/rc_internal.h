@@ -89,7 +89,25 @@ struct AttnParams {
     int* status;           // device status word
 };
 
+// K6: the copy-based window (an ablation): in every layer, slot s of the
+// destination bank takes slot (s + k) mod C of the source bank.
+struct ShiftParams {
+    const uint8_t* kc_src;     // all layers [L][H][T][128][D]
+    uint8_t* kc_dst;
+    const uint8_t* vt_src;     // all layers [L][H][T][D][128]
+    uint8_t* vt_dst;
+    const float* sk_src;       // [L][H][Cpad]
+    float* sk_dst;
+    const float* sv_src;
+    float* sv_dst;
+    const int32_t* grp_src;    // [L][Cpad]
+    int32_t* grp_dst;
+    int L, H, C, T, Cpad;
+    int k;                     // 0 < k < C
+};
+
 cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t s);
+cudaError_t launch_window_shift(const ShiftParams& p, int D, cudaStream_t s);
 cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s);
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status);
 cudaError_t launch_readtime(const ReadtimeParams& p, int D, cudaStream_t s);

@@ -61,6 +61,10 @@ extern "C" {
 /* Keep the unrotated bf16 K, V of every slot as well, so that rc_attend_readtime
    can redo RoPE and quantisation of the whole cache at read time. */
 #define RC_F_READTIME_ABLATION 1u
+/* Allocate a second bank of rings so that rc_cache_window_shift can move the
+   stored tokens the way a concatenating cache would (the copy-based window
+   ablation; doubles the ring memory; not combinable with the flag above). */
+#define RC_F_COPY_WINDOW 2u
 
 typedef struct rc_config {
     int layers;       /* attention layers with one ring each (>= 1) */
@@ -110,6 +114,23 @@ int rc_cache_write(rc_cache *h, int layer, const void *K_bf16, const void *V_bf1
  * write positions move by delta too.  delta = 0 is a no-op.
  */
 int rc_cache_delta_rotate(rc_cache *h, int64_t delta, void *stream);
+
+/*
+ * The copy-based window, an ablation of the ring (paperdot abstract: the
+ * window advances "without copies"; this is the copy).  A cache that keeps
+ * its tokens in position order moves them k slots down when k new positions
+ * arrive, then writes the new tokens at the end.  This call does that move in
+ * every layer: slot s takes what slot (s + k) mod slots held (K and V codes,
+ * their scales and write groups, one read and one write of every ring, into
+ * the second bank), and from then on a token at position p lives in slot
+ * floormod(p - delta_total - (sum of shifts), slots).  The set of stored
+ * tokens, their codes and every attention result are those of the ring;
+ * rc_cache_export returns the slots in their shifted order.  k = 0 (or a
+ * multiple of slots) moves nothing.
+ * Errors: RC_ERR_STATE unless the cache was created with RC_F_COPY_WINDOW;
+ * RC_ERR_ARG for a NULL handle or k < 0.
+ */
+int rc_cache_window_shift(rc_cache *h, int64_t k, void *stream);
 
 /*
  * Attention call (paperdot abstract: the new tokens' queries read the whole

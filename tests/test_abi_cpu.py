@@ -48,6 +48,8 @@ def test_bad_config_rejected_before_device_work(rc):
     cfg = rc._binding.rc_config(1, 2, 64, 64, 65, 10000.0, 0)      # max_write > slots
     assert rc.lib.rc_cache_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == rc.RC_ERR_ARG
     assert rc.lib.rc_cache_create(None, 0, ctypes.byref(h)) == rc.RC_ERR_ARG
+    cfg = rc._binding.rc_config(1, 2, 64, 64, 64, 10000.0, rc.RC_F_READTIME_ABLATION | rc.RC_F_COPY_WINDOW)
+    assert rc.lib.rc_cache_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == rc.RC_ERR_UNSUPPORTED
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
@@ -60,5 +62,6 @@ def test_null_handle_calls_are_rejected(rc):
     assert rc.lib.rc_cache_write(None, 0, None, None, None, 1, None) == rc.RC_ERR_ARG
     assert rc.lib.rc_attend(None, 0, None, None, 1, None) == rc.RC_ERR_ARG
     assert rc.lib.rc_cache_delta_rotate(None, 5, None) == rc.RC_ERR_ARG
+    assert rc.lib.rc_cache_window_shift(None, 5, None) == rc.RC_ERR_ARG
     assert rc.lib.rc_cache_sync(None) == rc.RC_ERR_ARG
     rc.lib.rc_cache_destroy(None)

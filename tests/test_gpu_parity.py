@@ -133,6 +133,74 @@ def test_split_tiles(rc, D):
     pr.attend_check(0, q)
 
 
+def _rolled(st: dict, r: int) -> dict:
+    """An exported layer state with its slot axis rotated: slot s takes slot (s + r) mod C."""
+    out = {}
+    for k, v in st.items():
+        out[k] = np.roll(v, -r, axis=1 if k in ("kcodes", "kscale", "vcodes", "vscale") else 0)
+    return out
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_copy_window(rc, D):
+    # The copy-based window: shifts of the slot axis (k = 37, 123, C - 1, C)
+    # between writes (one that wraps), a delta and attends.  The GPU state is
+    # the oracle's with the slot axis rotated by the sum of the shifts, and
+    # attention equals the oracle's.  C = 300 is not a multiple of 16, so the
+    # shifted V chunks straddle the ring's end and its padding.
+    H, C = 3, 300
+    g = rc.RingKVCache(2, H, D, C, max_write=C, copy_window=True)
+    o = oracle.OracleCache(2, H, D, C)
+    shift = 0
+
+    def write(layer, p0, n, seed):
+        k = si.normal_bf16(n, H, D, seed, "cuda")
+        v = si.normal_bf16(n, H, D, seed + 1, "cuda")
+        g.write(layer, k, v, np.arange(p0, p0 + n))
+        o.write(layer, k.cpu(), v.cpu(), np.arange(p0, p0 + n))
+
+    def check(what):
+        g.sync()
+        for layer in range(2):
+            check_state(g.export(layer), _rolled(o.export(layer), shift % C), f"{what}, layer {layer}")
+
+    def attend(layer, seed):
+        q = si.normal_bf16(len(o.last_positions(layer)), H, D, seed, "cuda")
+        gpu_attend_vs_oracle(g, layer, q, o.last_positions(layer))
+
+    def window_shift(k):
+        nonlocal shift
+        g.window_shift(k)
+        shift += k
+
+    write(0, 0, 200, 1100)
+    write(1, 0, 150, 1110)
+    check("first writes")
+    attend(0, 1120)
+    window_shift(37)
+    check("shift 37")
+    attend(0, 1121)
+    write(0, 200, 100, 1130)
+    check("write after shift")
+    attend(0, 1131)
+    window_shift(123)
+    write(1, 150, 271, 1140)   # wraps and overwrites the oldest slots
+    check("wrapping write after shift 123")
+    attend(1, 1141)
+    g.delta_rotate(-100)
+    o.delta_rotate(-100)
+    check("delta")
+    attend(0, 1150)
+    window_shift(C - 1)
+    write(0, 300, 57, 1160)
+    check("write after shift C - 1")
+    attend(0, 1161)
+    window_shift(C)            # moves nothing
+    check("shift C")
+    attend(1, 1170)
+    g.close()
+
+
 def test_production_call(rc):
     t = si.production_tensors(11, "cuda")
     C = si.PROD_SLOTS
