@@ -97,6 +97,25 @@ def _load():
         lib.orc_last_n.restype = i32
         lib.orc_last_pos.argtypes = [P, i32, P]
         lib.orc_last_pos.restype = None
+        # the bf16 cache
+        lib.orc_bf16_encode.argtypes = [f64]
+        lib.orc_bf16_encode.restype = ctypes.c_uint16
+        lib.orc_b_create.argtypes = [i32, i32, i32, i32, f64]
+        lib.orc_b_create.restype = P
+        lib.orc_b_destroy.argtypes = [P]
+        lib.orc_b_destroy.restype = None
+        lib.orc_b_write.argtypes = [P, i32, P, P, P, i32]
+        lib.orc_b_write.restype = i32
+        lib.orc_b_delta_rotate.argtypes = [P, i64]
+        lib.orc_b_delta_rotate.restype = None
+        lib.orc_b_attend.argtypes = [P, i32, P, i32, P]
+        lib.orc_b_attend.restype = i32
+        lib.orc_b_export.argtypes = [P, i32, P, P, P, P]
+        lib.orc_b_export.restype = None
+        lib.orc_b_last_n.argtypes = [P, i32]
+        lib.orc_b_last_n.restype = i32
+        lib.orc_b_last_pos.argtypes = [P, i32, P]
+        lib.orc_b_last_pos.restype = None
         _lib = lib
         return lib
 
@@ -128,6 +147,11 @@ def e4m3_encode(x: float) -> int:
 
 def e4m3_decode_all() -> np.ndarray:
     return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def bf16_encode(x: float) -> int:
+    """bf16 bits of x rounded once from fp64, to nearest with ties to even."""
+    return int(_load().orc_bf16_encode(float(x)))
 
 
 def rope_theta(i: int, d: int, base: float = 10000.0) -> float:
@@ -271,4 +295,62 @@ class OracleCache:
         out = np.zeros(n, np.int64)
         if n:
             self._lib.orc_last_pos(self._h, layer, _ptr(out))
+        return out
+
+
+class OracleBf16Cache:
+    """The same ring with bf16 storage (the non-FP8 cache): a write stores
+    RoPE(K) rounded once to bf16 and V as given; a delta rotation re-rotates
+    every stored key in fp64 and rounds it back to bf16; attention reads the
+    stored values.  Slots, positions and write serials as in OracleCache."""
+
+    def __init__(self, layers: int, heads: int, head_dim: int, slots: int, rope_base: float = 10000.0):
+        self._lib = _load()
+        self.L, self.H, self.d, self.C = layers, heads, head_dim, slots
+        self.base = rope_base
+        self._h = self._lib.orc_b_create(layers, heads, head_dim, slots, rope_base)
+        if not self._h:
+            raise ValueError("bad oracle cache shape")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.orc_b_destroy(h)
+            self._h = None
+
+    def write(self, layer: int, K, V, positions) -> None:
+        kb, vb = _bf16_bits(K), _bf16_bits(V)
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        n = pos.shape[0]
+        assert kb.shape == (n, self.H, self.d) and vb.shape == kb.shape
+        if self._lib.orc_b_write(self._h, layer, _ptr(kb), _ptr(vb), _ptr(pos), n) != 0:
+            raise ValueError("oracle write rejected (layer, n or duplicate slot)")
+
+    def delta_rotate(self, delta: int) -> None:
+        self._lib.orc_b_delta_rotate(self._h, int(delta))
+
+    def attend(self, layer: int, Q) -> np.ndarray:
+        qb = _bf16_bits(Q)
+        n = qb.shape[0]
+        out = np.zeros((n, self.H, self.d), dtype=np.float64)
+        rc = self._lib.orc_b_attend(self._h, layer, _ptr(qb), n, _ptr(out))
+        if rc == -1:
+            raise ValueError("bad attend arguments")
+        if rc == -2:
+            raise RuntimeError("attend: query count differs from the last write, or layer empty")
+        return out
+
+    def export(self, layer: int) -> dict:
+        H, C, d = self.H, self.C, self.d
+        st = dict(kbits=np.zeros((H, C, d), np.uint16), vbits=np.zeros((H, C, d), np.uint16),
+                  pos=np.zeros(C, np.int64), gid=np.zeros(C, np.int64))
+        self._lib.orc_b_export(self._h, layer, _ptr(st["kbits"]), _ptr(st["vbits"]), _ptr(st["pos"]),
+                               _ptr(st["gid"]))
+        return st
+
+    def last_positions(self, layer: int) -> np.ndarray:
+        n = self._lib.orc_b_last_n(self._h, layer)
+        out = np.zeros(n, np.int64)
+        if n:
+            self._lib.orc_b_last_pos(self._h, layer, _ptr(out))
         return out

@@ -524,3 +524,204 @@ void orc_readtime_image(int H, int d, int C, double base, const uint16_t *kraw,
     }
     free(xk); free(xv); free(occ);
 }
+
+/* ================================================================ bf16 cache
+ *
+ * The same ring with bf16 storage instead of E4M3 codes and scales: the
+ * non-FP8 cache that the pages compare the FP8 cache against (cpdf.ai blog,
+ * section "Blackwell, escalabilidade e limites do decodificador").  A write
+ * stores RoPE(K) rounded once from fp64 to bf16 (nearest, ties to even) and
+ * V as given (already bf16); a delta rotation decodes each stored key,
+ * rotates it by delta in fp64 and rounds it back to bf16; attention reads the
+ * stored values.  The slot, position and write-serial bookkeeping is that of
+ * the FP8 cache above.
+ */
+
+/* bf16 bits of x rounded to nearest, ties to even (8 significant bits; the
+   bf16 subnormals below 2^-126 step by 2^-133).  Magnitudes that round to
+   2^128 or more give infinity. */
+uint16_t orc_bf16_encode(double x)
+{
+    if (x != x)
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);                      /* a = m 2^e, m in [0.5, 1) */
+    int qe = e - 8;                    /* bf16 step in the binade [2^(e-1), 2^e) */
+    if (qe < -133)
+        qe = -133;                     /* subnormal range: fixed step 2^-133 */
+    double q = ldexp(a, -qe);          /* exact: a / step */
+    double r = nearbyint(q);           /* ties to even in the default mode */
+    double v = ldexp(r, qe);
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    float f = (float)v;                /* exact: at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+typedef struct orc_bcache {
+    int L, H, d, C;
+    double base;
+    uint16_t *kb, *vb;     /* [L][H][C][d] bf16 bits */
+    int64_t *pos;          /* [L][C] position of the stored token, or ORC_EMPTY */
+    int64_t *gid;          /* [L][C] serial number of the write that filled the slot */
+    int64_t *last_pos;     /* [L][C] positions of the layer's last write */
+    int *last_n;           /* [L] */
+    int64_t delta_total;
+    int64_t next_gid;
+} orc_bcache;
+
+orc_bcache *orc_b_create(int L, int H, int d, int C, double base)
+{
+    if (L <= 0 || H <= 0 || d <= 0 || (d % 2) != 0 || C <= 0)
+        return NULL;
+    orc_bcache *c = (orc_bcache *)calloc(1, sizeof *c);
+    c->L = L; c->H = H; c->d = d; c->C = C; c->base = base;
+    size_t nval = (size_t)L * H * C * d;
+    c->kb = (uint16_t *)calloc(nval, sizeof(uint16_t));
+    c->vb = (uint16_t *)calloc(nval, sizeof(uint16_t));
+    c->pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)L * C);
+    c->gid = (int64_t *)malloc(sizeof(int64_t) * (size_t)L * C);
+    c->last_pos = (int64_t *)calloc((size_t)L * C, sizeof(int64_t));
+    c->last_n = (int *)calloc((size_t)L, sizeof(int));
+    for (size_t i = 0; i < (size_t)L * C; ++i) {
+        c->pos[i] = ORC_EMPTY;
+        c->gid[i] = ORC_EMPTY;
+    }
+    return c;
+}
+
+void orc_b_destroy(orc_bcache *c)
+{
+    if (!c) return;
+    free(c->kb); free(c->vb); free(c->pos); free(c->gid); free(c->last_pos); free(c->last_n);
+    free(c);
+}
+
+#define IDX_B(c, l, h, s) ((((size_t)(l) * (c)->H + (h)) * (c)->C + (s)) * (c)->d)
+
+/* Write n tokens to layer l (K, V bf16 bits [n][H][d]).  Returns 0, or -1 on
+   bad arguments (n or layer out of range, two tokens on one slot). */
+int orc_b_write(orc_bcache *c, int l, const uint16_t *K, const uint16_t *V, const int64_t *positions, int n)
+{
+    if (!c || l < 0 || l >= c->L || n <= 0 || n > c->C)
+        return -1;
+    int H = c->H, d = c->d;
+    int64_t *slot = (int64_t *)malloc(sizeof(int64_t) * n);
+    char *seen = (char *)calloc((size_t)c->C, 1);
+    for (int t = 0; t < n; ++t) {
+        slot[t] = floormod(positions[t] - c->delta_total, c->C);
+        if (seen[slot[t]]) {
+            free(slot); free(seen);
+            return -1;
+        }
+        seen[slot[t]] = 1;
+    }
+    free(seen);
+    double *x = (double *)malloc(sizeof(double) * d);
+    for (int t = 0; t < n; ++t)
+        for (int h = 0; h < H; ++h) {
+            size_t src = ((size_t)t * H + h) * d;
+            for (int i = 0; i < d; ++i)
+                x[i] = orc_bf16_to_double(K[src + i]);
+            orc_rope_rotate(x, d, positions[t], c->base);
+            uint16_t *kd = c->kb + IDX_B(c, l, h, slot[t]);
+            for (int i = 0; i < d; ++i)
+                kd[i] = orc_bf16_encode(x[i]);
+            memcpy(c->vb + IDX_B(c, l, h, slot[t]), V + src, sizeof(uint16_t) * d);
+        }
+    for (int t = 0; t < n; ++t) {
+        c->pos[(size_t)l * c->C + slot[t]] = positions[t];
+        c->gid[(size_t)l * c->C + slot[t]] = c->next_gid;
+        c->last_pos[(size_t)l * c->C + t] = positions[t];
+    }
+    c->last_n[l] = n;
+    c->next_gid += 1;
+    free(x); free(slot);
+    return 0;
+}
+
+/* Every stored key of every layer: decode, rotate by delta (fp64), round to bf16. */
+void orc_b_delta_rotate(orc_bcache *c, int64_t delta)
+{
+    int C = c->C, d = c->d;
+    double *x = (double *)malloc(sizeof(double) * d);
+    for (int l = 0; l < c->L; ++l) {
+        for (int s = 0; s < C; ++s) {
+            if (c->pos[(size_t)l * C + s] == ORC_EMPTY) continue;
+            for (int h = 0; h < c->H; ++h) {
+                uint16_t *kd = c->kb + IDX_B(c, l, h, s);
+                for (int i = 0; i < d; ++i)
+                    x[i] = orc_bf16_to_double(kd[i]);
+                orc_rope_rotate(x, d, delta, c->base);
+                for (int i = 0; i < d; ++i)
+                    kd[i] = orc_bf16_encode(x[i]);
+            }
+            c->pos[(size_t)l * C + s] += delta;
+        }
+        for (int t = 0; t < c->last_n[l]; ++t)
+            c->last_pos[(size_t)l * C + t] += delta;
+    }
+    c->delta_total += delta;
+    free(x);
+}
+
+/* Attention of layer l's last-write queries Q (bf16 bits [n][H][d]) over the
+   stored values; out fp64 [n][H][d].  Returns 0, -1 on bad arguments, -2 if
+   n differs from the layer's last write or the layer is empty. */
+int orc_b_attend(const orc_bcache *c, int l, const uint16_t *Q, int n, double *out)
+{
+    if (!c || l < 0 || l >= c->L || n <= 0)
+        return -1;
+    if (c->last_n[l] == 0 || n != c->last_n[l])
+        return -2;
+    int H = c->H, d = c->d, C = c->C, m = 0;
+    for (int s = 0; s < C; ++s)
+        if (c->pos[(size_t)l * C + s] != ORC_EMPTY) ++m;
+    double *k = (double *)malloc(sizeof(double) * (size_t)m * d);
+    double *v = (double *)malloc(sizeof(double) * (size_t)m * d);
+    double *q = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *o = (double *)malloc(sizeof(double) * (size_t)n * d);
+    for (int h = 0; h < H; ++h) {
+        int j = 0;
+        for (int s = 0; s < C; ++s) {
+            if (c->pos[(size_t)l * C + s] == ORC_EMPTY) continue;
+            const uint16_t *kd = c->kb + IDX_B(c, l, h, s), *vd = c->vb + IDX_B(c, l, h, s);
+            for (int i = 0; i < d; ++i) {
+                k[(size_t)j * d + i] = orc_bf16_to_double(kd[i]);
+                v[(size_t)j * d + i] = orc_bf16_to_double(vd[i]);
+            }
+            ++j;
+        }
+        for (int t = 0; t < n; ++t)
+            for (int i = 0; i < d; ++i)
+                q[(size_t)t * d + i] = orc_bf16_to_double(Q[((size_t)t * H + h) * d + i]);
+        orc_rope_rows(q, n, d, c->last_pos + (size_t)l * C, c->base);
+        orc_attention_rows(q, n, k, v, m, d, o);
+        for (int t = 0; t < n; ++t)
+            memcpy(out + ((size_t)t * H + h) * d, o + (size_t)t * d, sizeof(double) * d);
+    }
+    free(k); free(v); free(q); free(o);
+    return 0;
+}
+
+/* Layer l's state: K, V bf16 bits [H][C][d], pos/gid [C]. */
+void orc_b_export(const orc_bcache *c, int l, uint16_t *kb, uint16_t *vb, int64_t *pos, int64_t *gid)
+{
+    size_t nv = (size_t)c->H * c->C * c->d;
+    if (kb) memcpy(kb, c->kb + IDX_B(c, l, 0, 0), nv * sizeof(uint16_t));
+    if (vb) memcpy(vb, c->vb + IDX_B(c, l, 0, 0), nv * sizeof(uint16_t));
+    if (pos) memcpy(pos, c->pos + (size_t)l * c->C, sizeof(int64_t) * c->C);
+    if (gid) memcpy(gid, c->gid + (size_t)l * c->C, sizeof(int64_t) * c->C);
+}
+
+int orc_b_last_n(const orc_bcache *c, int l) { return c->last_n[l]; }
+void orc_b_last_pos(const orc_bcache *c, int l, int64_t *out)
+{
+    memcpy(out, c->last_pos + (size_t)l * c->C, sizeof(int64_t) * c->last_n[l]);
+}
