@@ -2,8 +2,10 @@
 
 A plain fp64 C implementation (``rc_oracle.c``) of what the cache computes:
 the ring-slot map, write-time RoPE and per-head E4M3 quantisation, the delta
-rotation on a position reset, and softmax attention over the dequantised cache.
-This module compiles it with gcc and wraps it with ctypes.
+rotation on a position reset, and softmax attention over the dequantised cache
+(``OracleCache``); and the same ring with bf16 storage, the non-FP8 cache of
+the pages' comparison (``OracleBf16Cache``).  This module compiles it with gcc
+and wraps it with ctypes.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of
 ``bench.py`` may import this package.  It shares no code with the CUDA library

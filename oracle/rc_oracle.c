@@ -41,6 +41,9 @@
  * Everything here is fp64 except the stored fp32 scales and the 8-bit codes,
  * which are part of the state the method defines.  Every floating-point
  * operation is done in the order written, with no blocking or fusion.
+ *
+ * The end of the file holds a second state machine, the same ring with bf16
+ * storage (the non-FP8 cache of the pages' comparison), prefixed orc_b_.
  */
 #include <math.h>
 #include <stdint.h>
