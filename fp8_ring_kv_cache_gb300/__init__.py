@@ -2,6 +2,20 @@
 
 The compute path is the CUDA library librc.so (C ABI in include/rc.h); this
 package only binds it.  Build it with ``fp8_ring_kv_cache_gb300.build.build()``.
+
+Use (K, V, Q: CUDA bf16 tensors [n][heads][head_dim]; out: CUDA fp32, same shape)::
+
+    import numpy as np, torch
+    import fp8_ring_kv_cache_gb300 as rc
+
+    cache = rc.RingKVCache(layers=60, heads=48, head_dim=128, slots=5788)
+    cache.write(layer, K, V, np.arange(p0, p0 + n))  # RoPE + per-head E4M3, once
+    cache.attend(layer, Q, out)                      # Q = the last write's tokens
+    cache.delta_rotate(-757)                         # positions reset: keys re-rotated in place
+    cache.sync()                                     # raises RcError on a kernel error
+
+Every call is stream-ordered on torch's current stream (or ``stream=``); no
+call after construction allocates device memory.
 """
 from ._binding import (  # noqa: F401
     EMPTY, RC_ERR_ARG, RC_ERR_CUDA, RC_ERR_OOM, RC_ERR_STATE, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED,
