@@ -43,12 +43,11 @@ WRITE_BYTES = N_NEW * H * D * (2 + 2) + N_NEW * H * D * 2  # bf16 K,V read + E4M
 ROTATE_BYTES = 2.0 * L * H * C * D                        # K codes read + written, all layers
 READTIME_EXTRA_BYTES = C * H * D * (2 + 2) + C * H * D * 2  # bf16 store read + FP8 ring written
 
-# dram bytes per launch measured by ncu (profiles/), valid only for the kernel
-# source they were taken on
+# dram bytes per launch measured by ncu, valid only for the kernel source they
+# were taken on
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
-    # the production call (ncu, profiles/attn_kernel_production_call.md), valid
-    # while rc_attention.cu has this hash
+    # the production call, valid while rc_attention.cu has this hash
     "attention": {"bytes": 87.54e6,
                   "src_sha256": "dff29bc3193b23431ee739c502109a235ee9cea4afd9c66da51d77ea8881250a"},
 }
@@ -244,7 +243,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         return None
 
     peaks, peak_src = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]           # fp8 dense = 2x bf16 dense (nominal ratio)
+    # fp8 dense = 2x bf16 dense (nominal ratio).  The attention kernel is timed
+    # per launch (microseconds, full SM clock), so the burst rate applies; the
+    # fraction against the sustained (power-capped) rate is reported beside it.
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    fp8_peak_sustained = 2.0 * peaks["bf16_tflops_sustained"]
     hbm = peaks["hbm_gbs"]
     ms_step = elapsed_ms / args.steps
     value = job_throughput(world, args.steps, elapsed_ms)
@@ -280,7 +283,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "bound": "tensor", "kernel": "attention (rc_attend)",
             "achieved": round(achieved_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved_tflops / fp8_peak, 4), "traffic": traffic,
-            "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal ratio 2)",
+            "peak_source": f"{peak_src}: 2 x bf16_tflops, the burst rate (fp8/bf16 nominal ratio 2)",
+            "frac_of_sustained_peak": round(achieved_tflops / fp8_peak_sustained, 4),
             "per_launch_us": round(att_us, 3), "flop_per_launch": ATTN_FLOP,
         },
         "kernels": {
@@ -292,7 +296,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                              "gbs": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9, 1),
                              "frac_hbm": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9 / hbm, 4)},
             "attention": {"us": round(att_us, 3), "tflops": round(achieved_tflops, 1),
-                          "frac_fp8": round(achieved_tflops / fp8_peak, 4)},
+                          "frac_fp8": round(achieved_tflops / fp8_peak, 4),
+                          "frac_fp8_sustained": round(achieved_tflops / fp8_peak_sustained, 4)},
             "readtime_ablation": ab,
             "hbm_peak_gbs": hbm, "peak_source": peak_src,
         },
@@ -595,11 +600,13 @@ def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
 
 
 def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
-    """The same chunk through the public API with pinned host inputs: every call
-    copies its K, V, Q host->device and its output device->host, inside the
-    timed region.  Inputs go up on one copy stream and outputs come down on
-    another (the two directions run at once), each three buffers deep, so the
-    copies of neighbouring calls overlap the compute stream."""
+    """The same step as the device-timed one (a 240-call chunk, then the
+    60-layer delta rotation that restarts the window) through the public API
+    with pinned host inputs: every call copies its K, V, Q host->device and its
+    output device->host, inside the timed region.  Inputs go up on one copy
+    stream and outputs come down on another (the two directions run at once),
+    each three buffers deep, so the copies of neighbouring calls overlap the
+    compute stream."""
     import numpy as np
     import torch
 
@@ -654,6 +661,7 @@ def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
                 down.wait_event(out_ready[b])
                 hout[b].copy_(dout[b], non_blocking=True)
                 drained[b].record(down)
+        cache.delta_rotate(-N_NEW)          # the window restarts, as in the device-timed step
 
     for _ in range(args.warmup):
         chunk()

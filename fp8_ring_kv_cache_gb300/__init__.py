@@ -1,7 +1,7 @@
 """Write-time FP8 ring KV cache for one GB300 (sm_103a).
 
 The compute path is the CUDA library librc.so (C ABI in include/rc.h); this
-package only binds it.  Build it with ``fp8_ring_kv_cache_gb300.build.build()``.
+package only binds it.  Build it with ``python fp8_ring_kv_cache_gb300/build.py`` (or ``__graft_entry__.build()``).
 
 Use (K, V, Q: CUDA bf16 tensors [n][heads][head_dim]; out: CUDA fp32, same shape)::
 

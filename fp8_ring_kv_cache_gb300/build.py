@@ -1,7 +1,7 @@
 """Build librc.so (the C ABI of include/rc.h) in-tree with nvcc for sm_103a.
 
 Each .cu translation unit compiles in parallel; the shared library links the
-CUDA runtime statically.  Run: python -m fp8_ring_kv_cache_gb300.build
+CUDA runtime statically.  Run: python fp8_ring_kv_cache_gb300/build.py [--force] [-v]
 """
 from __future__ import annotations
 

@@ -825,14 +825,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
 
 template <int D>
 static cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t s) {
-    static bool configured = false;
+    static std::atomic<uint64_t> configured{0};
     constexpr uint32_t smem = AttnLayout<D>::kAlloc;
     static_assert(smem <= 227 * 1024, "attention shared memory over the sm_103 limit");
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = smem_limit_once(attn_kernel<D>, smem, configured);
+    if (e != cudaSuccess) return e;
     dim3 grid((p.n + kRowsPerCta - 1) / kRowsPerCta, p.H);
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
     return cudaGetLastError();

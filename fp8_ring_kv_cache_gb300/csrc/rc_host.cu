@@ -54,11 +54,11 @@ struct rc_cache {
     float* d_sk = nullptr;
     float* d_sv = nullptr;
     int32_t* d_grp = nullptr;
-    double* d_theta = nullptr;
     int* d_status = nullptr;
     __nv_bfloat16* d_kraw = nullptr;
     __nv_bfloat16* d_vraw = nullptr;
-    float2* d_slot_rope = nullptr;
+    int64_t* d_slot_pos = nullptr;   // [L][Cpad] each slot's current position (read-time store)
+    float2* d_rt_rope = nullptr;     // [Cpad][D/2] the read-time call's angle table
     uint8_t* d_rt_kc = nullptr;
     uint8_t* d_rt_vt = nullptr;
     float* d_rt_sk = nullptr;
@@ -111,11 +111,11 @@ void free_all(rc_cache* h) {
     cudaFree(h->d_sk);
     cudaFree(h->d_sv);
     cudaFree(h->d_grp);
-    cudaFree(h->d_theta);
     cudaFree(h->d_status);
     cudaFree(h->d_kraw);
     cudaFree(h->d_vraw);
-    cudaFree(h->d_slot_rope);
+    cudaFree(h->d_slot_pos);
+    cudaFree(h->d_rt_rope);
     cudaFree(h->d_rt_kc);
     cudaFree(h->d_rt_vt);
     cudaFree(h->d_rt_sk);
@@ -197,7 +197,7 @@ int rope_entry(rc_cache* h, const int64_t* p, int n, cudaStream_t s, int* err) {
     r.valid = false;
     RopeTableParams tp{};
     tp.table = r.d_table;
-    tp.theta = h->d_theta;
+    for (int i = 0; i < h->D / 2; ++i) tp.theta[i] = h->theta[i];
     tp.n = n;
     tp.half = h->D / 2;
     if (arith) {
@@ -302,7 +302,6 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     st |= dmalloc(&h->d_sk, sc);
     st |= dmalloc(&h->d_sv, sc);
     st |= dmalloc(&h->d_grp, static_cast<size_t>(h->L) * h->Cpad);
-    st |= dmalloc(&h->d_theta, static_cast<size_t>(h->D / 2));
     st |= dmalloc(&h->d_status, 1);
     for (auto& e : h->pool) {
         st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
@@ -315,7 +314,8 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
         const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
         st |= dmalloc(&h->d_kraw, raw);
         st |= dmalloc(&h->d_vraw, raw);
-        st |= dmalloc(&h->d_slot_rope, static_cast<size_t>(h->L) * h->Cpad * (h->D / 2));
+        st |= dmalloc(&h->d_slot_pos, static_cast<size_t>(h->L) * h->Cpad);
+        st |= dmalloc(&h->d_rt_rope, static_cast<size_t>(h->Cpad) * (h->D / 2));
         const size_t one = static_cast<size_t>(h->H) * h->T * kTileSlots * h->D;
         st |= dmalloc(&h->d_rt_kc, one);
         st |= dmalloc(&h->d_rt_vt, one);
@@ -348,7 +348,8 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     if (ok && h->ablation) {
         const size_t raw = static_cast<size_t>(h->L) * h->H * h->Cpad * h->D;
         ok = cudaMemset(h->d_kraw, 0, raw * 2) == cudaSuccess && cudaMemset(h->d_vraw, 0, raw * 2) == cudaSuccess &&
-             cudaMemset(h->d_slot_rope, 0, sizeof(float2) * h->L * h->Cpad * (h->D / 2)) == cudaSuccess;
+             cudaMemset(h->d_slot_pos, 0, sizeof(int64_t) * h->L * h->Cpad) == cudaSuccess &&
+             cudaMemset(h->d_rt_rope, 0, sizeof(float2) * h->Cpad * (h->D / 2)) == cudaSuccess;
         // the read-time ring's padding slots, like the main ring's, hold zero codes
         const size_t one = static_cast<size_t>(h->H) * h->T * kTileSlots * h->D;
         ok = ok && cudaMemset(h->d_rt_kc, 0, one) == cudaSuccess && cudaMemset(h->d_rt_vt, 0, one) == cudaSuccess &&
@@ -357,8 +358,6 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     }
     h->theta.resize(h->D / 2);
     for (int i = 0; i < h->D / 2; ++i) h->theta[i] = std::pow(cfg->rope_base, -2.0 * i / h->D);
-    ok = ok && cudaMemcpy(h->d_theta, h->theta.data(), sizeof(double) * (h->D / 2), cudaMemcpyHostToDevice) ==
-                   cudaSuccess;
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_all(h);
@@ -466,7 +465,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
         const size_t raw = static_cast<size_t>(layer) * h->H * h->Cpad * h->D;
         wp.kraw = h->d_kraw + raw;
         wp.vraw = h->d_vraw + raw;
-        wp.slot_rope = h->d_slot_rope + static_cast<size_t>(layer) * h->Cpad * (h->D / 2);
+        wp.slot_pos = h->d_slot_pos + static_cast<size_t>(layer) * h->Cpad;
     }
     if (launch_write(wp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
@@ -489,6 +488,8 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
     rp.kc = h->d_kc;
     rp.sk = h->d_sk;
     rp.grp = h->d_grp;
+    rp.slot_pos = h->ablation ? h->d_slot_pos : nullptr;
+    rp.delta = delta;
     rp.H = h->H;
     rp.C = h->C;
     rp.T = h->T;
@@ -583,11 +584,22 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     const size_t lsc = static_cast<size_t>(layer) * h->H * h->Cpad;
     AttnParams ap{};
     if (readtime) {
+        // RoPE at every slot's current position: the angle table of this call
+        // (fp64 angles, as for a write) from the device copy of the positions
+        RopeTableParams tp{};
+        tp.table = h->d_rt_rope;
+        tp.pos = h->d_slot_pos + static_cast<size_t>(layer) * h->Cpad;
+        tp.p0 = 0;
+        for (int i = 0; i < h->D / 2; ++i) tp.theta[i] = h->theta[i];
+        tp.n = h->C;
+        tp.half = h->D / 2;
+        if (launch_rope_table(tp, s) != cudaSuccess) return RC_ERR_CUDA;
+        h->launches += 1;
         ReadtimeParams rp{};
         const size_t raw = static_cast<size_t>(layer) * h->H * h->Cpad * h->D;
         rp.kraw = h->d_kraw + raw;
         rp.vraw = h->d_vraw + raw;
-        rp.slot_rope = h->d_slot_rope + static_cast<size_t>(layer) * h->Cpad * (h->D / 2);
+        rp.slot_rope = h->d_rt_rope;
         rp.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
         rp.kc = h->d_rt_kc;
         rp.vt = h->d_rt_vt;

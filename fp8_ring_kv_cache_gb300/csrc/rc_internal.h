@@ -4,9 +4,25 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace rc {
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute is held per device, so `done` keeps one bit per
+// device index (below 64; other devices set it on every launch).
+template <typename Kernel>
+inline cudaError_t smem_limit_once(Kernel* kernel, uint32_t bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 constexpr int kMaxHalfDim = 64;  // head_dim <= 128
 
@@ -15,9 +31,9 @@ struct RopeTableParams {
     float2* table;         // [n][D/2] (cos, sin)
     const int64_t* pos;    // device positions, or nullptr for p0 + t
     int64_t p0;
-    const double* theta;   // [D/2] fp64 frequencies
     int n;
     int half;              // D/2
+    double theta[kMaxHalfDim];  // fp64 frequencies theta_i (by value: no device copy)
 };
 
 // K2: fused RoPE + per-head amax + E4M3 quantisation + scatter into ring slots.
@@ -38,7 +54,7 @@ struct WriteParams {
     int32_t group;         // compact write-group index of this write
     __nv_bfloat16* kraw;   // read-time store [H][Cpad][D] (nullptr if off)
     __nv_bfloat16* vraw;
-    float2* slot_rope;     // read-time store [Cpad][D/2] (nullptr if off)
+    int64_t* slot_pos;     // read-time store: each slot's position [Cpad] (nullptr if off)
     int* status;           // device status word (bounded waits)
 };
 
@@ -47,6 +63,8 @@ struct RotateParams {
     uint8_t* kc;           // all layers [L][H][T][128][D]
     float* sk;             // [L][H][Cpad]
     const int32_t* grp;    // [L][Cpad]
+    int64_t* slot_pos;     // read-time store [L][Cpad]: moved by delta (nullptr if off)
+    int64_t delta;
     int H, C, T, Cpad;
     float2 cs[kMaxHalfDim];  // (cos, sin) of delta * theta_i
 };
@@ -56,7 +74,7 @@ struct RotateParams {
 struct ReadtimeParams {
     const __nv_bfloat16* kraw;  // layer [H][Cpad][D]
     const __nv_bfloat16* vraw;
-    const float2* slot_rope;    // layer [Cpad][D/2]
+    const float2* slot_rope;    // [Cpad][D/2]: cos/sin at each slot's current position
     const int32_t* grp;         // layer [Cpad]
     uint8_t* kc;                // scratch ring [H][T][128][D]
     uint8_t* vt;                // [H][T][D][128]

@@ -1,9 +1,10 @@
 // rc_noalloc.cu -- rc_ring_write_noalloc: the write path (RoPE table kernel +
 // fused RoPE/amax/E4M3 write kernel) for callers that cannot allocate device
 // memory.  The caller owns the ring buffers and passes them in; the one piece
-// of scratch the write needs -- the per-token cos/sin table, plus the RoPE
-// frequencies and a copy of non-arithmetic positions -- lives in a file-scope
-// __device__ array instead of memory from cudaMalloc.
+// of scratch the write needs -- the per-token cos/sin table, plus a copy of
+// non-arithmetic positions -- lives in a file-scope __device__ array instead
+// of memory from cudaMalloc.  The RoPE frequencies travel in the kernel's
+// parameters.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -18,8 +19,7 @@ namespace {
 
 constexpr int kNoallocMaxTokens = RC_NOALLOC_MAX_TOKENS;
 constexpr int kNoallocMaxHalf = 64;  // head_dim <= 128
-constexpr size_t kThetaOff = 0;
-constexpr size_t kPosOff = 512;     // after 64 doubles
+constexpr size_t kPosOff = 0;
 constexpr size_t kTableOff = kPosOff + sizeof(int64_t) * kNoallocMaxTokens;
 constexpr size_t kScratchBytes = kTableOff + sizeof(float2) * kNoallocMaxTokens * kNoallocMaxHalf;
 constexpr int kMaxDevices = 64;
@@ -31,7 +31,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 namespace {
 
-// Device address of g_noalloc_scratch on each device, found once per device.
+// Device address of g_noalloc_scratch on each device, found once per device
+// (by the first call made with that device current).  A cudaDeviceReset of
+// the device after that call would leave the address stale; it is not
+// supported.
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
 
 int scratch_for_current_device(unsigned char** out) {
@@ -75,12 +78,6 @@ extern "C" int rc_ring_write_noalloc(const rc_ring_view* ring, const void* K_bf1
     if (st != RC_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    double theta[kNoallocMaxHalf];
-    for (int i = 0; i < half; ++i) theta[i] = std::pow(rope_base, -2.0 * i / D);
-    // pageable host source: the call returns once the bytes have been staged
-    if (cudaMemcpyAsync(scratch + kThetaOff, theta, sizeof(double) * half, cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
-        return RC_ERR_CUDA;
     bool arith = true;
     for (int t = 1; t < n; ++t)
         if (positions[t] != positions[0] + t) {
@@ -88,6 +85,7 @@ extern "C" int rc_ring_write_noalloc(const rc_ring_view* ring, const void* K_bf1
             break;
         }
     int64_t* dpos = reinterpret_cast<int64_t*>(scratch + kPosOff);
+    // pageable host source: the call returns once the positions have been staged
     if (!arith && cudaMemcpyAsync(dpos, positions, sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return RC_ERR_CUDA;
     float2* table = reinterpret_cast<float2*>(scratch + kTableOff);
@@ -96,7 +94,7 @@ extern "C" int rc_ring_write_noalloc(const rc_ring_view* ring, const void* K_bf1
     tp.table = table;
     tp.pos = arith ? nullptr : dpos;
     tp.p0 = positions[0];
-    tp.theta = reinterpret_cast<const double*>(scratch + kThetaOff);
+    for (int i = 0; i < half && i < kNoallocMaxHalf; ++i) tp.theta[i] = std::pow(rope_base, -2.0 * i / D);
     tp.n = n;
     tp.half = half;
     if (launch_rope_table(tp, s) != cudaSuccess) return RC_ERR_CUDA;

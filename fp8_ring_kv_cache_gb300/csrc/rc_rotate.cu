@@ -13,7 +13,9 @@
 // K5 readtime_kernel (the original read-time design the abstract and the
 //    cpdf.ai section "Como rodar 57B em tempo real com batch size 1" describe):
 //    rebuilds one layer's FP8 ring from the unrotated bf16 store -- RoPE at each
-//    slot's position, one amax per head for K and for V over the whole cache,
+//    slot's CURRENT position (the angle table of the call is built just before
+//    by K1 from the device copy of the slots' positions, which every delta
+//    moves), one amax per head for K and for V over the whole cache,
 //    quantisation -- into a scratch ring that the attention kernel then reads.
 #include "rc_device.cuh"
 #include "rc_internal.h"
@@ -203,6 +205,12 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
             *reinterpret_cast<uint4*>(chunk_addr(r)) = make_uint4(w[0], w[1], w[2], w[3]);
             if (chunk == 0) gsk[r] = s_new;
         }
+    }
+    // the read-time ablation's copy of each slot's position moves with it
+    if (p.slot_pos != nullptr && h == 0) {
+        int64_t* spos = p.slot_pos + static_cast<size_t>(l) * p.Cpad + row0;
+        for (int r = tid; r < nrows; r += kRotThreads)
+            if (ggrp[r] >= 0) spos[r] += p.delta;
     }
 }
 

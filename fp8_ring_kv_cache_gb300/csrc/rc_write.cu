@@ -19,13 +19,18 @@
 
 namespace rc {
 
-__global__ void rope_table_kernel(RopeTableParams p) {
+__global__ void __launch_bounds__(256) rope_table_kernel(RopeTableParams p) {
+    // the frequencies go through shared memory: lanes index different ones,
+    // which the parameter bank would serve one address at a time
+    __shared__ double th[kMaxHalfDim];
+    if (threadIdx.x < p.half) th[threadIdx.x] = p.theta[threadIdx.x];
+    __syncthreads();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= p.n * p.half) return;
     const int t = idx / p.half;
     const int i = idx - t * p.half;
     const int64_t pos = p.pos ? p.pos[t] : p.p0 + t;
-    const double ang = static_cast<double>(pos) * p.theta[i];
+    const double ang = static_cast<double>(pos) * th[i];
     double s, c;
     sincos(ang, &s, &c);
     p.table[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
@@ -155,7 +160,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
                     amv = fmaxf(amv, fabsf(v[e]));
                 }
                 if (p.kraw != nullptr && warp + kWriteWarps * i < cnt) {
-                    // read-time ablation store: the unrotated bf16 row and its angles
+                    // read-time ablation store: the unrotated bf16 row and the slot's position
                     const int slot = slot_of(tb + tl);
                     const size_t dst = (static_cast<size_t>(h) * p.Cpad + slot) * D + dim0;
 #pragma unroll
@@ -163,12 +168,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
                         p.kraw[dst + e] = kbuf[tl * D + dim0 + e];
                         p.vraw[dst + e] = vbuf[tl * D + dim0 + e];
                     }
-                    if (h == 0) {
-#pragma unroll
-                        for (int j = 0; j < EPL / 2; ++j)
-                            p.slot_rope[static_cast<size_t>(slot) * HALF + dim0 / 2 + j] =
-                                p.rope[static_cast<size_t>(tb + tl) * HALF + dim0 / 2 + j];
-                    }
+                    if (h == 0 && lane == 0) p.slot_pos[slot] = p.pos ? p.pos[tb + tl] : p.p0 + tb + tl;
                 }
             }
         }
@@ -283,13 +283,10 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
 
 template <int D>
 static cudaError_t launch_write_d(const WriteParams& p, cudaStream_t s) {
-    static bool configured = false;
+    static std::atomic<uint64_t> configured{0};
     constexpr uint32_t smem = WriteSmem<D>::kTotal;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(write_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = smem_limit_once(write_kernel<D>, smem, configured);
+    if (e != cudaSuccess) return e;
     dim3 grid(kWriteCluster, p.H);
     write_kernel<D><<<grid, kWriteThreads, smem, s>>>(p);
     return cudaGetLastError();

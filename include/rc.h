@@ -151,6 +151,11 @@ int rc_attend(rc_cache *h, int layer, const void *Q_bf16, float *out_f32, int n,
  * com batch size 1": RoPE and FP8 quantisation of the WHOLE cache redone in
  * every attention call).  Rebuilds this layer's FP8 ring from the unrotated
  * bf16 store into a scratch ring, then runs the same attention kernel on it.
+ * Every stored key is rotated at its slot's CURRENT position: the store keeps
+ * each slot's position on the device and rc_cache_delta_rotate moves it, so
+ * after any number of resets the read-time ring holds the keys the write-time
+ * ring would hold had it been written at today's positions.  Each call first
+ * rebuilds the angle table of all slots (fp64 angles) from those positions.
  * Requires RC_F_READTIME_ABLATION, else RC_ERR_STATE.  The read-time ring
  * quantises each head with ONE scale over all occupied slots (per K and V),
  * so its codes differ from the write-time ring's wherever that ring holds
@@ -201,22 +206,26 @@ int rc_cache_export_readtime(rc_cache *h, uint8_t *kcodes, float *kscale,
  * can synchronise the whole device.  rc_ring_write_noalloc serves them: it
  * performs exactly the write of rc_cache_write (RoPE table kernel, then the
  * fused RoPE + per-head amax + E4M3 write kernel) into ring buffers that the
- * CALLER owns, and it allocates nothing.  Its only scratch -- the RoPE
- * frequencies, a copy of non-arithmetic positions and the per-token cos/sin
- * table -- lives in one file-scope __device__ array of about 2 MiB
- * (RC_NOALLOC_MAX_TOKENS tokens x 64 pairs x 8 bytes, plus 33 KiB), which
- * every GPU that loads the library holds until the process exits.
+ * CALLER owns, and it allocates nothing.  Its only scratch -- a copy of
+ * non-arithmetic positions and the per-token cos/sin table -- lives in one
+ * file-scope __device__ array of about 2 MiB (RC_NOALLOC_MAX_TOKENS tokens x
+ * 64 pairs x 8 bytes, plus 32 KiB), which every GPU that loads the library
+ * holds until the process exits.  The RoPE frequencies go to the kernel as
+ * parameters.
  *
  * Rules:
  *   - n <= RC_NOALLOC_MAX_TOKENS, else RC_ERR_ARG (nothing is launched).
  *   - The first call on a device looks up the array's device address on the
- *     current device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *     current device (cudaGetSymbolAddress) and keeps it; make that first call
+ *     before any stream capture.  Resetting that device (cudaDeviceReset)
+ *     afterwards is not supported: the kept address would be stale.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents.  Calls that overlap on the GPU (other streams or
  *     threads without ordering) race on it; order them on one stream.
- *   - positions is a HOST array; a non-arithmetic run is copied into the
- *     array from pageable memory (the call returns once it is staged).
+ *   - positions is a HOST array.  An arithmetic run p0, p0+1, ... needs no
+ *     copy; any other position vector is copied into the array from the
+ *     caller's (pageable) memory with cudaMemcpyAsync, which returns once the
+ *     bytes are staged.
  *   - The caller keeps the ring state: delta_total (the sum of resets applied
  *     to this ring) and a write-group index in [0, slots) unique among the
  *     ring's live groups.  There is no delta rotation or attention entry on a

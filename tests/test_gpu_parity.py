@@ -338,3 +338,58 @@ def test_readtime_ablation(rc):
                                   o.export(0)["pos"], q.cpu(), pos)
         check_attention(out_rt.cpu().numpy(), ref, "read-time attention")
         assert torch.isfinite(out_wt).all()
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_readtime_after_resets(rc, D):
+    """The read-time ablation after position resets: every key of the whole
+    cache is rotated at its slot's CURRENT position in each call.  Sequence:
+    write, delta, a write that wraps, read-time attention, a second delta (the
+    window restarts at 0), read-time attention again; the read-time ring and
+    the output are compared with the oracle's read-time image built from the
+    unrotated keys at the positions the oracle's state machine holds."""
+    H, C = 4, 700
+    g = rc.RingKVCache(1, H, D, C, readtime_ablation=True)
+    o = oracle.OracleCache(1, H, D, C)
+    kraw = torch.zeros(H, C, D, dtype=torch.bfloat16)
+    vraw = torch.zeros(H, C, D, dtype=torch.bfloat16)
+
+    def write(p0, n, seed):
+        k = si.normal_bf16(n, H, D, seed, "cuda", mult=torch.full((H, 1), 1.5))
+        v = si.normal_bf16(n, H, D, seed + 1, "cuda")
+        pos = np.arange(p0, p0 + n)
+        g.write(0, k, v, pos)
+        o.write(0, k.cpu(), v.cpu(), pos)
+        slots = [o.slot_of(x) for x in pos]
+        kraw[:, slots] = k.cpu().permute(1, 0, 2)
+        vraw[:, slots] = v.cpu().permute(1, 0, 2)
+        return pos
+
+    def check(q, what):
+        n = q.shape[0]
+        out = torch.empty(n, H, D, dtype=torch.float32, device="cuda")
+        g.attend_readtime(0, q, out)
+        g.sync()
+        img = g.export_readtime()
+        st = o.export(0)
+        assert np.array_equal(g.export(0)["pos"], st["pos"]), f"{what}: positions"
+        want = oracle.readtime_image(kraw, vraw, st["pos"])
+        occ = st["pos"] != oracle.EMPTY
+        check_codes(img["kcodes"][:, occ], want["kcodes"][:, occ], f"{what}: read-time K codes")
+        check_codes(img["vcodes"][:, occ], want["vcodes"][:, occ], f"{what}: read-time V codes")
+        check_scales(img["kscale"][:, occ], want["kscale"][:, occ], f"{what}: read-time K scales")
+        check_scales(img["vscale"][:, occ], want["vscale"][:, occ], f"{what}: read-time V scales")
+        ref = oracle.attend_image(img["kcodes"], img["kscale"], img["vcodes"], img["vscale"], st["pos"],
+                                  q.cpu(), o.last_positions(0))
+        check_attention(out.cpu().numpy(), ref, f"{what}: read-time attention")
+
+    write(0, 500, 7100)
+    g.delta_rotate(-123_457)
+    o.delta_rotate(-123_457)
+    pos = write(500 - 123_457, 450, 7200)          # wraps onto slots 0..249
+    check(si.normal_bf16(len(pos), H, D, 7300, "cuda"), "after one reset")
+    oldest = int(o.export(0)["pos"][o.export(0)["pos"] != oracle.EMPTY].min())
+    g.delta_rotate(-oldest)
+    o.delta_rotate(-oldest)
+    check(si.normal_bf16(len(pos), H, D, 7400, "cuda"), "after the window restart")
+    g.close()

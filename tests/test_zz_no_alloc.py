@@ -102,3 +102,41 @@ def test_noalloc_rejects_oversize():
     with pytest.raises(rc.RcError) as e:
         rc_ring_write_noalloc(ring, k, k, np.arange(n), delta_total=0, group=0)
     assert e.value.status == rc.RC_ERR_ARG
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_noalloc_permuted_positions_after_reset(D):
+    """A write whose positions are not an arithmetic run (they are copied into
+    the static array) into a ring whose positions were reset (nonzero
+    delta_total), against rc_cache_write after the same reset.  The caller-owned
+    ring has no delta rotation, so the comparison covers the slots of the write
+    made after the reset."""
+    import fp8_ring_kv_cache_gb300 as rc
+    from fp8_ring_kv_cache_gb300._binding import rc_ring_write_noalloc
+
+    H, C, delta = 6, 900, -100_003
+    cache = rc.RingKVCache(1, H, D, C)
+    ring = _new_ring(H, D, C)
+    k0 = si.normal_bf16(700, H, D, 9300, "cuda")
+    v0 = si.normal_bf16(700, H, D, 9301, "cuda")
+    cache.write(0, k0, v0, np.arange(0, 700))
+    rc_ring_write_noalloc(ring, k0, v0, np.arange(0, 700), delta_total=0, group=0)
+    cache.delta_rotate(delta)
+    rng = np.random.default_rng(9302)
+    for i, (p0, n) in enumerate([(700 + delta, 500), (1200 + delta, 333)]):
+        pos = rng.permutation(np.arange(p0, p0 + n))      # wraps past slot 899 in the first write
+        k = si.normal_bf16(n, H, D, 9310 + i, "cuda", mult=torch.full((H, 1), 2.0))
+        v = si.normal_bf16(n, H, D, 9320 + i, "cuda")
+        cache.write(0, k, v, pos)
+        rc_ring_write_noalloc(ring, k, v, pos, delta_total=delta, group=1 + i)
+        torch.cuda.synchronize()
+        want = cache.export(0)
+        got = _canonical(ring, H, D, C)
+        slots = (pos - delta) % C
+        check_codes(got["kcodes"][:, slots], want["kcodes"][:, slots], f"write {i} K codes")
+        check_codes(got["vcodes"][:, slots], want["vcodes"][:, slots], f"write {i} V codes")
+        check_scales(got["kscale"][:, slots], want["kscale"][:, slots], f"write {i} K scales")
+        check_scales(got["vscale"][:, slots], want["vscale"][:, slots], f"write {i} V scales")
+        assert (got["group"][slots] == 1 + i).all()
+        assert np.array_equal(want["pos"][slots], pos)
+    cache.close()
