@@ -49,22 +49,32 @@ constexpr int kMTile = 128;
 constexpr int kRowsPerCta = 2 * kMTile;
 constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpSm0 = 2, kWarpCvt = 10, kCvtWarps = 2;
 constexpr uint32_t kTmemCols = 512;
-// The converted V tile holds code / 256 (the E4M3 bits placed in an fp16), so
-// O accumulates P V / 256; the epilogue multiplies the 256 back in.
-constexpr float kV16Scale = 256.f;
+// The converted V tile holds each code's value exactly in fp16 (every finite
+// E4M3 value is an fp16 value), so O accumulates P V as is.
 
-// barrier indices
+// mbarrier indices
 enum : int {
-    B_KV_FULL = 0,     // [kStages]
-    B_KV_EMPTY = 3,    // [kStages]
-    B_V16_FULL = 6,    // [2]
-    B_V16_EMPTY = 8,   // [2]
-    B_S_FULL = 10,     // [2]
-    B_P_FULL = 12,     // [2]
-    B_O_DONE = 14,     // [2]
-    B_DRAIN = 16,
-    B_COUNT = 17
+    B_KV_FULL = 0,     // [kStages] K tile and scales landed
+    B_KV_EMPTY = 2,    // [kStages] the MMA warp and the 8 softmax warps are done with the stage
+    B_V16_FULL = 4,    // [2] the converter warps filled the fp16 V buffer
+    B_V16_EMPTY = 6,   // [2] both P.V of a tile read the fp16 V buffer
+    B_S_FULL = 8,      // [2] scores of M tile i in TMEM
+    B_O_DONE = 10,     // [2]
+    B_DRAIN = 12,
+    B_COUNT = 13
 };
+static_assert(kStages == 2, "barrier layout assumes two K stages");
+// Named (hardware) barriers.  The MMA warp takes each P tile through a
+// rendezvous (bar.sync on both sides) instead of polling an mbarrier: the QK
+// MMA's operand reads fill the shared-memory pipe, so an mbarrier poll then
+// costs ~300 cycles, long enough for the tensor pipe to run dry behind a thread
+// whose issue is paced by the MMAs it queues.  Both sides block, so neither can
+// run a phase ahead.  The P0 rendezvous of tile t also stands for "fp16 V of
+// tile t converted" and "K tile t + 1 landed": one lane of softmax group 0
+// tests those mbarriers early in its softmax, so the MMA warp polls nothing.
+constexpr int kNbSoftmax = 1;  // the 8 softmax warps (the head's largest V scale)
+constexpr int kNbP = 2;        // [2] softmax group of M tile i with the MMA warp: P_i is in TMEM
+constexpr int kNbPThreads = 4 * 32 + 32;
 
 template <int D>
 struct AttnLayout {
@@ -99,14 +109,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortS
     return __all_sync(0xffffffffu, ok);
 }
 
-// Four E4M3 codes (one 32-bit word) -> four fp16 holding code / 256, exactly:
-// E4M3 s.eeee.mmm and fp16 s.eeeee.mmmmmmmmmm share the layout once the
-// magnitude bits sit at fp16 bits 7..13, and the exponent bias differs by 8.
-__device__ __forceinline__ void e4m3x4_to_f16x4_div256(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t a = __byte_perm(w, 0u, 0x1404);  // codes 0, 1 in bytes 1 and 3
-    const uint32_t b = __byte_perm(w, 0u, 0x3424);  // codes 2, 3 in bytes 1 and 3
-    lo = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
-    hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
+// Four E4M3 codes (one 32-bit word, code 0 in the low byte) -> four fp16 values,
+// exactly, with the hardware conversion (far fewer instructions than placing
+// the bits by hand, which matters on the schedulers the softmax warps share).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Softmax of the ring's last tile (fewer than 128 slots) when one write group
@@ -264,7 +276,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             mbar_init(&bars[B_V16_FULL + i], kCvtWarps);  // the converter warps
             mbar_init(&bars[B_V16_EMPTY + i], 1);
             mbar_init(&bars[B_S_FULL + i], 1);
-            mbar_init(&bars[B_P_FULL + i], 4);
             mbar_init(&bars[B_O_DONE + i], 1);
         }
         mbar_init(&bars[B_DRAIN], 1);
@@ -414,69 +425,88 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_qk = instr_desc(kFmtE4M3, kFmtE4M3, 128, 128);
-            const uint32_t idesc_pv = instr_desc(kFmtF16, kFmtF16, 128, D);
-            const uint32_t q_base = smem_u32(smem + Lay::kQ);
-            const uint32_t v16_base = smem_u32(smem + Lay::kV16);
-            auto issue_qk = [&](int i, int s) {
-                const uint32_t k_base = smem_u32(stage_ptr(s));
-                const uint32_t d_tmem = tmem + 128u * i;
+        // Lane 0 issues; the whole warp takes part in the rendezvous.
+        const uint32_t idesc_qk = instr_desc(kFmtE4M3, kFmtE4M3, 128, 128);
+        const uint32_t idesc_pv = instr_desc(kFmtF16, kFmtF16, 128, D);
+        // Base descriptors, built once: an operand's descriptor differs from its
+        // base only in the start-address field (bits 0..13, address / 16), and
+        // shared memory ends below 256 KB, so one add moves it without a carry
+        // into the other fields.  Issuing an MMA is then two adds and the
+        // instruction, which keeps this thread ahead of the tensor pipe while it
+        // shares its scheduler with two softmax warps.
+        const uint64_t dq0 = smem_desc(smem_u32(smem + Lay::kQ), 16, kSboK, kSwzK);
+        const uint64_t dk0 = smem_desc(smem_u32(stage_ptr(0)), 16, kSboK, kSwzK);
+        const uint64_t dv0 = smem_desc(smem_u32(smem + Lay::kV16), 16, 1024, 2);
+        auto issue_qk = [&](int i, int s) {
+            const uint32_t d_tmem = tmem + 128u * i;
+            const uint64_t qa = dq0 + static_cast<uint64_t>((i * kMTile * D) >> 4);
+            const uint64_t kb = dk0 + static_cast<uint64_t>((s * Lay::kStageBytes) >> 4);
 #pragma unroll
-                for (int pc = 0; pc < kQPieces; ++pc)
+            for (int pc = 0; pc < kQPieces; ++pc)
 #pragma unroll
-                    for (int k = 0; k < D / 32; ++k) {
-                        const uint64_t a = smem_desc(q_base + (pc * 2 + i) * (kMTile * D) + k * 32, 16, kSboK, kSwzK);
-                        const uint64_t b = smem_desc(k_base + k * 32, 16, kSboK, kSwzK);
-                        mma_f8_ss(d_tmem, a, b, idesc_qk, (pc | k) != 0);
-                    }
-            };
-            auto issue_pv = [&](int i, int jt, bool acc) {
-                const uint32_t d_tmem = tmem + 256u + static_cast<uint32_t>(D) * i;
-                const uint32_t a_tmem = tmem + 128u * i;
-                const uint32_t vb = v16_base + (jt & 1) * Lay::kV16One;
+                for (int k = 0; k < D / 32; ++k)
+                    mma_f8_ss(d_tmem, qa + ((pc * 2 * kMTile * D + k * 32) >> 4), kb + ((k * 32) >> 4), idesc_qk,
+                              (pc | k) != 0);
+        };
+        auto issue_pv = [&](int i, int jt, bool acc) {
+            const uint32_t d_tmem = tmem + 256u + static_cast<uint32_t>(D) * i;
+            const uint32_t a_tmem = tmem + 128u * i;
+            const uint64_t vb = dv0 + static_cast<uint64_t>(((jt & 1) * Lay::kV16One) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t b = smem_desc(vb + (kk >> 2) * (D * 128) + (kk & 3) * 32, 16, 1024, 2);
-                    mma_f16_ts(d_tmem, a_tmem + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            // A wait polls an mbarrier in shared memory, which the tensor core's
-            // operand reads keep busy: each is placed right after an issue, so
-            // it overlaps MMAs already queued.  Per tile j: PV0(j-1), [K tile
-            // j], QK0(j), [P1], PV1(j-1), QK1(j), [next tile's fp16 V].
-            auto v16_ready = [&](int jt) {
-                return mbar_wait(&bars[B_V16_FULL + (jt & 1)], (jt >> 1) & 1, ab, kDevTimeoutMma);
-            };
-            bool ok = true;
-            for (int j = 0; j < T && ok; ++j) {
-                const int s = j % kStages;
-                for (int i = 0; i < 2 && ok; ++i) {
-                    if (j > 0) {
-                        ok = mbar_wait(&bars[B_P_FULL + i], (j - 1) & 1, ab, kDevTimeoutMma);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(i, j - 1, j - 1 > 0);
-                        if (i == 1) mma_commit(&bars[B_V16_EMPTY + ((j - 1) & 1)]);
-                    }
-                    if (i == 0) {
-                        ok = mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutMma);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    issue_qk(i, s);
-                    mma_commit(&bars[B_S_FULL + i]);
-                }
-                if (ok) mma_commit(&bars[B_KV_EMPTY + s]);
-                if (ok) ok = v16_ready(j);  // for PV0(j) in the next round
-            }
-            for (int i = 0; i < 2 && ok; ++i) {
-                ok = mbar_wait(&bars[B_P_FULL + i], (T - 1) & 1, ab, kDevTimeoutMma);
-                if (!ok) break;
+            for (int kk = 0; kk < 8; ++kk)
+                mma_f16_ts(d_tmem, a_tmem + kk * 8, vb + (((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4), idesc_pv,
+                           (acc || kk > 0) ? 1u : 0u);
+        };
+        // K tile j has landed (lane 0 polls; the warp agrees)
+        auto kv_ready = [&](int j) -> bool {
+            bool r = true;
+            if (lane == 0) r = mbar_wait(&bars[B_KV_FULL + j % kStages], (j / kStages) & 1, ab, kDevTimeoutMma);
+            return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+        };
+        const bool leader = lane == 0;
+        bool ok = kv_ready(0);
+        if (ok && leader) {
+            tc_fence_after();
+            issue_qk(0, 0);
+            mma_commit(&bars[B_S_FULL + 0]);
+            issue_qk(1, 0);
+            mma_commit(&bars[B_S_FULL + 1]);
+            mma_commit(&bars[B_KV_EMPTY + 0]);
+        }
+        // Round j: P.V of tile j - 1 for both M tiles, Q.K of tile j (j < T):
+        // PV0(j-1), QK0(j), PV1(j-1), QK1(j).  Every round passes both
+        // rendezvous, also after an abort, so no partner is left waiting.
+        for (int j = 1; j <= T; ++j) {
+            const int s = j % kStages;
+            ok = named_barrier_and(kNbP + 0, kNbPThreads, ok);  // P0 and fp16 V of tile j - 1, K tile j
+            if (ok && leader) {
                 tc_fence_after();
-                issue_pv(i, T - 1, T - 1 > 0);
-                mma_commit(&bars[B_O_DONE + i]);
+                issue_pv(0, j - 1, j - 1 > 0);
             }
+            if (ok && leader) {
+                if (j < T) {
+                    tc_fence_after();
+                    issue_qk(0, s);
+                    mma_commit(&bars[B_S_FULL + 0]);
+                } else {
+                    mma_commit(&bars[B_O_DONE + 0]);
+                }
+            }
+            ok = named_barrier_and(kNbP + 1, kNbPThreads, ok);  // P1 of tile j - 1
+            if (ok && leader) {
+                tc_fence_after();
+                issue_pv(1, j - 1, j - 1 > 0);
+                mma_commit(&bars[B_V16_EMPTY + ((j - 1) & 1)]);
+                if (j < T) {
+                    issue_qk(1, s);
+                    mma_commit(&bars[B_S_FULL + 1]);
+                    mma_commit(&bars[B_KV_EMPTY + s]);
+                } else {
+                    mma_commit(&bars[B_O_DONE + 1]);
+                }
+            }
+        }
+        if (leader) {
             // every MMA has finished before the tensor memory is released
             mma_commit(&bars[B_DRAIN]);
             uint64_t t0 = global_timer_ns();
@@ -507,7 +537,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) reinterpret_cast<float*>(misc)[4 + warp - kWarpSm0] = m;
-            named_barrier_sync(1, 256);
+            named_barrier_sync(kNbSoftmax, 256);
         }
         float svmax = 0.f;
 #pragma unroll
@@ -517,11 +547,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         const float lsv = (svmax > 0.f) ? lg2_approx(svmax) : 0.f;
         const float2 a2 = make_float2(a, a);
         float m_run = -INFINITY, l_run = 0.f;
-        for (int j = 0; j < T && ok; ++j) {
+        const bool checker = mt == 0 && quad == 0 && lane == 0;  // lane 0 of warp 4
+        // softmax of tile j: P into TMEM (over S), O rescaled if the max moved
+        auto tile = [&](int j) -> bool {
             const int s = j % kStages;
             // the tile's scales land with its K tile, before its scores: read them first
-            ok = warp_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutSoftmax);
-            if (!ok) break;
+            if (!warp_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, ab, kDevTimeoutSoftmax)) return false;
             const uint8_t* st = stage_ptr(s);
             const float* ssk = reinterpret_cast<const float*>(st + Lay::kTile);
             const float* ssv = ssk + kTileSlots;
@@ -532,8 +563,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             const float cu = uni ? ssk[0] * a : 0.f;
             const float lsv0 = uni ? lg2_approx(ssv[0]) : 0.f;
             const float isv0 = uni ? ex2(-lsv0) : 1.f;
-            ok = warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax);
-            if (!ok) break;
+            // a two-run tile needs the scales of its first and last slot only
+            const int sb = uni ? 0 : static_cast<int>(p.split[j]);
+            const float cuA = ssk[0] * a, cuB = ssk[kTileSlots - 1] * a;
+            const float lvA = lg2_approx(ssv[0]), lvB = lg2_approx(ssv[kTileSlots - 1]);
+            // Uniform and two-run tiles read nothing more from the stage: release
+            // it before the scores arrive, so the loader can refill it a full
+            // tile period ahead of its next use.  Other tiles read per-slot
+            // scales during their softmax and release the stage after it.
+            const bool early_release = uni || sb != 0;
+            if (early_release) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_KV_EMPTY + s]);
+            }
+            // the checker lane: fp16 V of tile j and K tile j + 1 (tested now,
+            // the results are read after the softmax, so the shared-memory
+            // latency is hidden; a blocking wait follows only if they were late)
+            bool vk = true;
+            if (checker) {
+                vk = mbar_test(&bars[B_V16_FULL + (j & 1)], (j >> 1) & 1);
+                if (j + 1 < T) vk = mbar_test(&bars[B_KV_FULL + (j + 1) % kStages], ((j + 1) / kStages) & 1) && vk;
+            }
+            if (!warp_wait(&bars[B_S_FULL + mt], j & 1, ab, kDevTimeoutSoftmax)) return false;
             tc_fence_after();
 
             float m_new, alpha;
@@ -592,13 +643,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                             pk[k / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
                         }
                     };
+                    // P (128 slots as 64 fp16 pairs) goes to columns 0..63; the first
+                    // half's store is under way while the second half is computed
                     uint32_t pa[32], pb[32];
                     p_chunk(v0, pa);
                     p_chunk(v1, pa + 16);
+                    tmem_st32(s_tm, pa);
                     p_chunk(v2, pb);
                     p_chunk(v3, pb + 16);
-                    // P (128 slots as 64 fp16 pairs) goes to columns 0..63
-                    tmem_st32(s_tm, pa);
                     tmem_st32(s_tm + 32, pb);
             };
             // Split tile: slots [0, sb) belong to one write group (scales A) and
@@ -616,8 +668,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 tmem_ld32_async(s_tm + 32 * c1, v1);
                 tmem_ld32_async(s_tm + 32 * c2, v2);
                 tmem_ld32_async(s_tm + 32 * cs, v3);
-                const float cuA = ssk[0] * a, cuB = ssk[kTileSlots - 1] * a;
-                const float lvA = lg2_approx(ssv[0]), lvB = lg2_approx(ssv[kTileSlots - 1]);
                 tmem_wait_ld_dep(v0);
                 reg_fence(v1);
                 reg_fence(v2);
@@ -697,7 +747,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                     tmem_st16(s_tm + 16 * cs, pk);
                 }
             };
-            const int sb = uni ? 0 : static_cast<int>(p.split[j]);
             if (__builtin_expect(uni && nvalid == kTileSlots, 1)) {
                 uniform_tile();
             } else if (uni) {
@@ -714,8 +763,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 ls[0].x = r.z;
             }
             tmem_st_wait();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_KV_EMPTY + s]);
+            if (!early_release) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_KV_EMPTY + s]);
+            }
             // rescale the running output when the max moved (warp-uniform)
             if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
 #pragma unroll 1
@@ -733,15 +784,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
             l_run = l_run * alpha + lsum * isv0;
             m_run = m_new;
+            if (checker && !vk) {
+                if (!mbar_wait(&bars[B_V16_FULL + (j & 1)], (j >> 1) & 1, ab, kDevTimeoutSoftmax)) return false;
+                if (j + 1 < T &&
+                    !mbar_wait(&bars[B_KV_FULL + (j + 1) % kStages], ((j + 1) / kStages) & 1, ab, kDevTimeoutSoftmax))
+                    return false;
+            }
+            return true;
+        };
+        // every tile passes the P rendezvous with the MMA warp, also after an abort
+        for (int j = 0; j < T; ++j) {
+            if (ok) ok = tile(j);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_P_FULL + mt]);
+            ok = named_barrier_and(kNbP + mt, kNbPThreads, ok);
         }
         // ------------------------------------------------------------ epilogue
         if (ok) ok = warp_wait(&bars[B_O_DONE + mt], 0, ab, kDevTimeoutEpilogue);
         if (ok) {
             tc_fence_after();
-            const float fin = (l_run > 0.f) ? kV16Scale / l_run : 0.f;
+            const float fin = (l_run > 0.f) ? 1.f / l_run : 0.f;
             float* orow = p.out + (static_cast<size_t>(grow) * p.H + h) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -774,42 +836,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
             for (int k = 0; k < kHalf; ++k)
                 r[k] = ldg_nc_na_v4(src + (ct + kCvtThreads * ((hh & 1) * kHalf + k)) * 16);
         };
-        auto convert = [&](int hh, const uint4 (&r)[kHalf]) -> bool {
+        bool cok = true;
+        // converts half hh of the tile stream; the second half of a tile
+        // publishes the buffer
+        auto convert = [&](int hh, const uint4 (&r)[kHalf]) {
             const int jt = hh >> 1, b = jt & 1;
-            if ((hh & 1) == 0 &&
-                !warp_wait(&bars[B_V16_EMPTY + b], ((jt >> 1) & 1) ^ 1, ab, kDevTimeoutConvert))
-                return false;
+            if ((hh & 1) == 0 && cok)
+                cok = warp_wait(&bars[B_V16_EMPTY + b], ((jt >> 1) & 1) ^ 1, ab, kDevTimeoutConvert);
             uint8_t* dstb = v16 + b * Lay::kV16One;
 #pragma unroll
-            for (int k = 0; k < kHalf; ++k) {
+            for (int k = 0; k < kHalf && cok; ++k) {
                 const int u = ct + kCvtThreads * ((hh & 1) * kHalf + k);
                 const int rr = u >> 3, cp = u & 7;
                 const int c = cp ^ (rr & 7);  // logical 16-slot chunk
                 uint32_t o[8];
-                e4m3x4_to_f16x4_div256(r[k].x, o[0], o[1]);
-                e4m3x4_to_f16x4_div256(r[k].y, o[2], o[3]);
-                e4m3x4_to_f16x4_div256(r[k].z, o[4], o[5]);
-                e4m3x4_to_f16x4_div256(r[k].w, o[6], o[7]);
+                e4m3x4_to_f16x4(r[k].x, o[0], o[1]);
+                e4m3x4_to_f16x4(r[k].y, o[2], o[3]);
+                e4m3x4_to_f16x4(r[k].z, o[4], o[5]);
+                e4m3x4_to_f16x4(r[k].w, o[6], o[7]);
                 uint8_t* dst = dstb + (c >> 2) * (D * 128) + rr * 128;
                 const int l0 = 2 * (c & 3);
                 *reinterpret_cast<uint4*>(dst + (((l0) ^ (rr & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4*>(dst + (((l0 + 1) ^ (rr & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
-            if (hh & 1) {
+            if ((hh & 1) && cok) {
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_V16_FULL + b]);
             }
-            return true;
         };
         uint4 ra[kHalf], rb[kHalf];
         const int nh = 2 * T;
         if (nh > 0) fetch(0, ra);
         for (int hh = 0; hh < nh; hh += 2) {
             fetch(hh + 1, rb);
-            if (!convert(hh, ra)) break;
+            convert(hh, ra);
             if (hh + 2 < nh) fetch(hh + 2, ra);
-            if (!convert(hh + 1, rb)) break;
+            convert(hh + 1, rb);
         }
     }
 

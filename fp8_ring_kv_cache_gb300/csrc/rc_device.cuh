@@ -75,6 +75,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test: has the phase with the given parity of `bar` completed?
+// (The result can be consumed well after the test is issued.)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Abort state shared by all threads of a CTA: a kernel that gives up a wait
 // records where in *status (global) and raises `flag` so every role leaves
 // its loop and the CTA can release its tensor memory and exit.
@@ -106,6 +120,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, AbortS
 // Barrier `id` (1..15) among `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// The same barrier, returning the AND of `pred` over all `count` threads (every
+// participant of a barrier instance uses this form).
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %3, 0;\n\t"
+        "bar.red.and.pred po, %1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+        : "memory");
+    return r != 0;
 }
 
 // 16-byte read-only global load that does not allocate in L1 (the data is
