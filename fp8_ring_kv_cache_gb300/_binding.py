@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_occupancy": ([P, I], I),
         "rc_cache_delta_total": ([P], I64),
         "rc_cache_launch_count": ([P], I64),
+        "rc_cache_set_wait_limit": ([P, ctypes.c_uint64], I),
         "rc_tile_kinds": ([P, I, P, P], I),
         "rc_ring_write_noalloc": ([ctypes.POINTER(rc_ring_view), P, P, P, I, I64, ctypes.c_int32,
                                    ctypes.c_double, P], I),
@@ -216,6 +217,10 @@ def rc_cache_launch_count(h) -> int:
     return int(lib.rc_cache_launch_count(h))
 
 
+def rc_cache_set_wait_limit(h, ns: int) -> None:
+    _check(lib.rc_cache_set_wait_limit(h, int(ns)), "rc_cache_set_wait_limit")
+
+
 class RingKVCache:
     """Owns one rc_cache handle; methods forward to the C entry points."""
 
@@ -269,6 +274,9 @@ class RingKVCache:
     @property
     def launch_count(self):
         return rc_cache_launch_count(self.handle)
+
+    def set_wait_limit(self, ns):
+        rc_cache_set_wait_limit(self.handle, ns)
 
 
 RC_NOALLOC_MAX_TOKENS = 4096

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     const int h = blockIdx.y;
     const int row0 = blockIdx.x * kRowsPerCta;
     const int T = p.T;
-    AbortState ab{reinterpret_cast<volatile uint32_t*>(&misc[2]), p.status};
+    AbortState ab{reinterpret_cast<volatile uint32_t*>(&misc[2]), p.status, p.wait_ns};
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {

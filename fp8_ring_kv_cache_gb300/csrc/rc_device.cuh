@@ -95,22 +95,36 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 struct AbortState {
     volatile uint32_t* flag;  // shared memory
     int* status;              // global memory (0 = ok), or nullptr
+    uint64_t limit_ns;        // how long one wait may take before the CTA gives up
 };
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; kernels take microseconds
+// The default wait limit (kernels take microseconds), and the fixed bound of
+// the teardown drains, which must outlast any MMA or copy still in flight.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ void abort_wait(AbortState ab, int where) {
+    *ab.flag = 1;
+    if (ab.status != nullptr) atomicCAS(ab.status, 0, where);
+}
 
 // Wait until the phase with the given parity of `bar` has completed.  Returns
-// false if the CTA is aborting or the wait ran past kWaitLimitNs.
+// false if the CTA is aborting or the wait ran past ab.limit_ns.  A limit of 0
+// gives up at once on a phase not already complete (a non-blocking test: the
+// failure-path tests use it to make a wait run out).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, AbortState ab, int where) {
+    if (ab.limit_ns == 0) {
+        if (mbar_test(bar, parity)) return true;
+        abort_wait(ab, where);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31) == 0) {
             if (*ab.flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *ab.flag = 1;
-                if (ab.status != nullptr) atomicCAS(ab.status, 0, where);
+            if (global_timer_ns() - t0 > ab.limit_ns) {
+                abort_wait(ab, where);
                 return false;
             }
         }

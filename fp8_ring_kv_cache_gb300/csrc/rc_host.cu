@@ -11,6 +11,7 @@
 #include <array>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -89,6 +90,7 @@ struct rc_cache {
     // slot floormod(p - delta_total - slot_shift, C) (0 for a plain ring)
     int64_t slot_shift = 0;
     cudaStream_t last_stream = nullptr;
+    uint64_t wait_ns = 2000000000ull;  // limit of one bounded device wait (rc_cache_set_wait_limit)
 };
 
 namespace {
@@ -166,6 +168,25 @@ void refresh_uniform(rc_cache* h, int layer) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side fault injection for the failure-path tests, read from the
+// environment at each use: RC_FAULT_INJECT=alloc:K makes the K-th allocation
+// (1-based; device or pinned) of an rc_cache_create fail, RC_FAULT_INJECT=launch
+// makes every entry point that launches kernels fail with RC_ERR_CUDA after its
+// argument checks and before it changes anything.  Unset: nothing is injected.
+struct FaultPlan {
+    int alloc_at = 0;
+    bool launch = false;
+};
+FaultPlan fault_plan() {
+    FaultPlan f;
+    const char* e = std::getenv("RC_FAULT_INJECT");
+    if (e == nullptr) return f;
+    if (std::strncmp(e, "alloc:", 6) == 0) f.alloc_at = std::atoi(e + 6);
+    if (std::strcmp(e, "launch") == 0) f.launch = true;
+    return f;
+}
+bool launch_fault() { return fault_plan().launch; }
 
 bool is_arith(const int64_t* p, int n) {
     for (int t = 1; t < n; ++t)
@@ -297,6 +318,10 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
 
     int st = RC_OK;
     const size_t rb = ring_bytes(h), sc = scale_count(h);
+    const FaultPlan fault = fault_plan();
+    int alloc_no = 0;
+    auto injected = [&]() { return fault.alloc_at > 0 && ++alloc_no == fault.alloc_at; };
+    auto dmalloc = [&](auto** p, size_t count) { return injected() ? RC_ERR_OOM : ::dmalloc(p, count); };
     st |= dmalloc(&h->d_kc, rb);
     st |= dmalloc(&h->d_vt, rb);
     st |= dmalloc(&h->d_sk, sc);
@@ -306,7 +331,8 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     for (auto& e : h->pool) {
         st |= dmalloc(&e.d_table, static_cast<size_t>(h->max_write) * (h->D / 2));
         st |= dmalloc(&e.d_pos, static_cast<size_t>(h->max_write));
-        if (cudaMallocHost(reinterpret_cast<void**>(&e.h_pos), sizeof(int64_t) * h->max_write) != cudaSuccess)
+        if (injected() ||
+            cudaMallocHost(reinterpret_cast<void**>(&e.h_pos), sizeof(int64_t) * h->max_write) != cudaSuccess)
             st |= RC_ERR_OOM;
         if (cudaEventCreateWithFlags(&e.copied, cudaEventDisableTiming) != cudaSuccess) st |= RC_ERR_OOM;
     }
@@ -398,6 +424,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
     if (!aligned16(K_bf16) || !aligned16(V_bf16)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
+    if (launch_fault()) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // distinct slots
     if (++h->mark == 0) {
@@ -481,6 +508,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
 int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
     if (!h) return RC_ERR_ARG;
     if (delta == 0) return RC_OK;
+    if (launch_fault()) return RC_ERR_CUDA;
     if (check_sticky() != RC_OK) return RC_ERR_CUDA;
     if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -519,6 +547,7 @@ int rc_cache_window_shift(rc_cache* h, int64_t k, void* stream) {
         h->slot_shift += k;
         return RC_OK;
     }
+    if (launch_fault()) return RC_ERR_CUDA;
     if (check_sticky() != RC_OK) return RC_ERR_CUDA;
     if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -566,6 +595,7 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     if (layer < 0 || layer >= h->L || n < 1) return RC_ERR_ARG;
     if (h->last_n[layer] == 0 || n != h->last_n[layer] || h->occupancy[layer] == 0) return RC_ERR_STATE;
     if (readtime && !h->ablation) return RC_ERR_STATE;
+    if (launch_fault()) return RC_ERR_CUDA;
     if (check_sticky() != RC_OK) return RC_ERR_CUDA;
     if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -649,6 +679,7 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     }
     ap.sm_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
     ap.status = h->d_status;
+    ap.wait_ns = h->wait_ns;
     if (launch_attention(ap, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
     h->last_stream = s;
@@ -751,6 +782,12 @@ int rc_cache_occupancy(const rc_cache* h, int layer) {
 }
 
 int64_t rc_cache_delta_total(const rc_cache* h) { return h ? h->delta_total : 0; }
+
+int rc_cache_set_wait_limit(rc_cache* h, uint64_t ns) {
+    if (!h || ns > 60000000000ull) return RC_ERR_ARG;
+    h->wait_ns = ns;
+    return RC_OK;
+}
 
 int64_t rc_cache_launch_count(const rc_cache* h) { return h ? h->launches : 0; }
 

@@ -105,6 +105,7 @@ struct AttnParams {
     uint8_t split[256];
     float sm_log2;         // log2(e) / sqrt(D)
     int* status;           // device status word
+    uint64_t wait_ns;      // limit of one bounded wait (0: give up on any phase not complete)
 };
 
 // K6: the copy-based window (an ablation): in every layer, slot s of the

@@ -177,6 +177,24 @@ const char *rc_status_string(int status);
 int rc_cache_sync(rc_cache *h);
 
 /*
+ * Failure-path support.  Every wait inside the attention kernel is bounded:
+ * past `ns` nanoseconds (default 2 s) the kernel gives up, records where, frees
+ * its tensor memory and returns, and the next rc_cache_sync reports
+ * RC_ERR_TIMEOUT (and clears the record; the ring itself is not modified by an
+ * attention call, so the handle stays usable).  ns = 0 gives up on any wait
+ * whose phase is not already complete, which makes a wait run out on purpose.
+ * Errors: RC_ERR_ARG for a NULL handle or ns above 60 s.
+ *
+ * Host-side fault injection, read from the environment at each use:
+ * RC_FAULT_INJECT=alloc:K makes the K-th allocation (1-based, device or
+ * pinned) of rc_cache_create fail, which then returns RC_ERR_OOM having freed
+ * everything it had allocated; RC_FAULT_INJECT=launch makes every call that
+ * launches kernels return RC_ERR_CUDA after its argument checks, before it
+ * changes anything.
+ */
+int rc_cache_set_wait_limit(rc_cache *h, uint64_t ns);
+
+/*
  * Copy ring `layer` to HOST buffers in canonical layout (synchronous):
  * kcodes, vcodes: uint8 [heads][slots][head_dim] E4M3 codes; kscale, vscale:
  * fp32 [heads][slots]; pos: int64 [slots] position (INT64_MIN = empty);
