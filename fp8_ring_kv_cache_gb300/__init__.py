@@ -14,14 +14,17 @@ Use (K, V, Q: CUDA bf16 tensors [n][heads][head_dim]; out: CUDA fp32, same shape
     cache.delta_rotate(-757)                         # positions reset: keys re-rotated in place
     cache.sync()                                     # raises RcError on a kernel error
 
+``RingKVCache(..., bf16_cache=True)`` keeps the same ring in bf16 (no scales):
+the non-FP8 side of the FP8-versus-bf16 cache comparison.
+
 Every call is stream-ordered on torch's current stream (or ``stream=``); no
 call after construction allocates device memory.
 """
 from ._binding import (  # noqa: F401
     EMPTY, RC_ERR_ARG, RC_ERR_CUDA, RC_ERR_OOM, RC_ERR_STATE, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED,
-    RC_F_COPY_WINDOW, RC_F_READTIME_ABLATION, RC_OK, RcError, RingKVCache, declared_symbols, lib, rc_attend, rc_attend_readtime,
+    RC_F_BF16_CACHE, RC_F_COPY_WINDOW, RC_F_READTIME_ABLATION, RC_OK, RcError, RingKVCache, declared_symbols, lib, rc_attend, rc_attend_readtime,
     rc_cache_create, rc_cache_delta_rotate, rc_cache_delta_total, rc_cache_destroy, rc_cache_export,
-    rc_cache_export_readtime, rc_cache_launch_count, rc_cache_occupancy, rc_cache_set_wait_limit, rc_cache_sync,
+    rc_cache_export_bf16, rc_cache_export_readtime, rc_cache_launch_count, rc_cache_occupancy, rc_cache_set_wait_limit, rc_cache_sync,
     rc_cache_write,
     rc_cache_window_shift, rc_tile_kinds,
     rc_status_string,

@@ -25,6 +25,7 @@ RC_ERR_TIMEOUT = -5
 RC_ERR_UNSUPPORTED = -6
 RC_F_READTIME_ABLATION = 1
 RC_F_COPY_WINDOW = 2
+RC_F_BF16_CACHE = 4
 EMPTY = np.iinfo(np.int64).min
 
 
@@ -64,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_sync": ([P], I),
         "rc_cache_export": ([P, I, P, P, P, P, P, P], I),
         "rc_cache_export_readtime": ([P, P, P, P, P], I),
+        "rc_cache_export_bf16": ([P, I, P, P, P, P], I),
         "rc_cache_occupancy": ([P, I], I),
         "rc_cache_delta_total": ([P], I64),
         "rc_cache_launch_count": ([P], I64),
@@ -193,6 +195,14 @@ def rc_cache_export_readtime(h, heads: int, head_dim: int, slots: int) -> dict:
     return st
 
 
+def rc_cache_export_bf16(h, layer: int, heads: int, head_dim: int, slots: int) -> dict:
+    st = dict(kbits=np.zeros((heads, slots, head_dim), np.uint16), vbits=np.zeros((heads, slots, head_dim), np.uint16),
+              pos=np.zeros(slots, np.int64), gid=np.zeros(slots, np.int64))
+    _check(lib.rc_cache_export_bf16(h, int(layer), *[_np_ptr(st[k]) for k in ("kbits", "vbits", "pos", "gid")]),
+           "rc_cache_export_bf16")
+    return st
+
+
 def rc_tile_kinds(grp) -> tuple[np.ndarray, np.ndarray]:
     """(uniform [4] uint64 bitmask, split [256] uint8) of a ring's slot groups."""
     g = np.ascontiguousarray(np.asarray(grp, dtype=np.int32))
@@ -226,10 +236,12 @@ class RingKVCache:
 
     def __init__(self, layers: int, heads: int, head_dim: int, slots: int, max_write: int | None = None,
                  rope_base: float = 10000.0, readtime_ablation: bool = False, device: int = 0,
-                 copy_window: bool = False):
+                 copy_window: bool = False, bf16_cache: bool = False):
         self.layers, self.heads, self.head_dim, self.slots = layers, heads, head_dim, slots
         self.max_write = slots if max_write is None else max_write
-        flags = (RC_F_READTIME_ABLATION if readtime_ablation else 0) | (RC_F_COPY_WINDOW if copy_window else 0)
+        flags = ((RC_F_READTIME_ABLATION if readtime_ablation else 0) | (RC_F_COPY_WINDOW if copy_window else 0) |
+                 (RC_F_BF16_CACHE if bf16_cache else 0))
+        self.bf16_cache = bf16_cache
         self.handle = rc_cache_create(layers, heads, head_dim, slots, self.max_write, rope_base, flags, device)
 
     def close(self) -> None:
@@ -259,6 +271,8 @@ class RingKVCache:
         rc_cache_sync(self.handle)
 
     def export(self, layer):
+        if self.bf16_cache:
+            return rc_cache_export_bf16(self.handle, layer, self.heads, self.head_dim, self.slots)
         return rc_cache_export(self.handle, layer, self.heads, self.head_dim, self.slots)
 
     def export_readtime(self):

@@ -103,11 +103,6 @@ __device__ __forceinline__ float split4(float x) {
     return __fsub_rn(c, __fsub_rn(c, x));
 }
 
-// Every lane waits; the warp continues only if all lanes saw the phase.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState ab, int where) {
-    const bool ok = mbar_wait(bar, parity, ab, where);
-    return __all_sync(0xffffffffu, ok);
-}
 
 // Four E4M3 codes (one 32-bit word, code 0 in the low byte) -> four fp16 values,
 // exactly, with the hardware conversion (far fewer instructions than placing

@@ -131,6 +131,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, AbortS
     }
 }
 
+// Every lane waits; the warp continues only if all lanes saw the phase.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState ab, int where) {
+    const bool ok = mbar_wait(bar, parity, ab, where);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Barrier `id` (1..15) among `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -221,7 +227,8 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
     return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4 operand format
-constexpr uint32_t kFmtF16 = 0;   // kind::f16 operand format (1 would be bf16)
+constexpr uint32_t kFmtF16 = 0;   // kind::f16 operand format: fp16
+constexpr uint32_t kFmtBF16 = 1;  // kind::f16 operand format: bf16
 
 // D[tmem] (+)= A[smem] * B[smem]^T, 8-bit operands.
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -230,6 +237,16 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t adesc, uint6
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit operands (f16 or bf16, both the same).
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

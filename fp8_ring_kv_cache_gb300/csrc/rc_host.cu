@@ -49,6 +49,7 @@ struct rc_cache {
     int L = 0, H = 0, D = 0, C = 0, T = 0, Cpad = 0, max_write = 0;
     bool ablation = false;
     bool copy_window = false;  // RC_F_COPY_WINDOW: a second bank for rc_cache_window_shift
+    bool bf16 = false;         // RC_F_BF16_CACHE: bf16 tiles in d_kc / d_vt, no scales
     // device memory
     uint8_t* d_kc = nullptr;
     uint8_t* d_vt = nullptr;
@@ -96,9 +97,9 @@ struct rc_cache {
 namespace {
 
 size_t ring_bytes(const rc_cache* h) {
-    return static_cast<size_t>(h->L) * h->H * h->T * kTileSlots * h->D;
+    return static_cast<size_t>(h->L) * h->H * h->T * kTileSlots * h->D * (h->bf16 ? 2 : 1);
 }
-size_t scale_count(const rc_cache* h) { return static_cast<size_t>(h->L) * h->H * h->Cpad; }
+size_t scale_count(const rc_cache* h) { return h->bf16 ? 0 : static_cast<size_t>(h->L) * h->H * h->Cpad; }
 
 int64_t floormod(int64_t a, int64_t m) {
     int64_t r = a % m;
@@ -295,6 +296,8 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     if (cfg->head_dim != 64 && cfg->head_dim != 128) return RC_ERR_UNSUPPORTED;
     if (cfg->slots > 32768 || cfg->heads > 65535 || cfg->layers > 65535) return RC_ERR_UNSUPPORTED;
     if ((cfg->flags & RC_F_READTIME_ABLATION) && (cfg->flags & RC_F_COPY_WINDOW)) return RC_ERR_UNSUPPORTED;
+    if ((cfg->flags & RC_F_BF16_CACHE) && (cfg->flags & (RC_F_READTIME_ABLATION | RC_F_COPY_WINDOW)))
+        return RC_ERR_UNSUPPORTED;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return RC_ERR_ARG;
     cudaDeviceProp prop{};
@@ -315,6 +318,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     h->max_write = cfg->max_write;
     h->ablation = (cfg->flags & RC_F_READTIME_ABLATION) != 0;
     h->copy_window = (cfg->flags & RC_F_COPY_WINDOW) != 0;
+    h->bf16 = (cfg->flags & RC_F_BF16_CACHE) != 0;
 
     int st = RC_OK;
     const size_t rb = ring_bytes(h), sc = scale_count(h);
@@ -467,12 +471,12 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     }
 
     WriteParams wp{};
-    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D;
+    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D * (h->bf16 ? 2 : 1);
     const size_t lsc = static_cast<size_t>(layer) * h->H * h->Cpad;
     wp.kc = h->d_kc + lring;
     wp.vt = h->d_vt + lring;
-    wp.sk = h->d_sk + lsc;
-    wp.sv = h->d_sv + lsc;
+    wp.sk = h->bf16 ? nullptr : h->d_sk + lsc;
+    wp.sv = h->bf16 ? nullptr : h->d_sv + lsc;
     wp.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
     wp.K = static_cast<const __nv_bfloat16*>(K_bf16);
     wp.V = static_cast<const __nv_bfloat16*>(V_bf16);
@@ -494,7 +498,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
         wp.vraw = h->d_vraw + raw;
         wp.slot_pos = h->d_slot_pos + static_cast<size_t>(layer) * h->Cpad;
     }
-    if (launch_write(wp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    if ((h->bf16 ? launch_bf16_write(wp, h->D, s) : launch_write(wp, h->D, s)) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
     h->last_pos[layer].assign(positions, positions + n);
     h->uniform_dirty[layer] = 1;
@@ -526,7 +530,9 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
         const double ang = static_cast<double>(delta) * h->theta[i];
         rp.cs[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
     }
-    if (launch_rotate(rp, h->D, h->L, s, h->d_status) != cudaSuccess) return RC_ERR_CUDA;
+    if ((h->bf16 ? launch_bf16_rotate(rp, h->D, h->L, s) : launch_rotate(rp, h->D, h->L, s, h->d_status)) !=
+        cudaSuccess)
+        return RC_ERR_CUDA;
     h->launches += 1;
     for (size_t i = 0; i < h->pos.size(); ++i)
         if (h->pos[i] != kEmpty) h->pos[i] += delta;
@@ -588,6 +594,50 @@ int rc_cache_window_shift(rc_cache* h, int64_t k, void* stream) {
     return RC_OK;
 }
 
+// The bf16 ring's attention call: every tile whose slots are all occupied takes
+// the fast path (no scales, no validity test).
+static int attend_bf16(rc_cache* h, int layer, const void* Q_bf16, float* out, int n, void* stream) {
+    if (check_sticky() != RC_OK) return RC_ERR_CUDA;
+    if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int entry = h->last_entry[layer];
+    if (entry < 0 || !h->pool[entry].valid || h->pool[entry].n != n || h->pool[entry].p0 != h->last_pos[layer][0] ||
+        (!h->pool[entry].arith && h->pool[entry].pos != h->last_pos[layer])) {
+        int err = RC_OK;
+        entry = rope_entry(h, h->last_pos[layer].data(), n, s, &err);
+        if (entry < 0) return err;
+        h->last_entry[layer] = entry;
+    }
+    const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D * 2;
+    AttnParams ap{};
+    ap.kc = h->d_kc + lring;
+    ap.vt = h->d_vt + lring;
+    ap.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
+    ap.q = static_cast<const __nv_bfloat16*>(Q_bf16);
+    ap.rope = h->pool[entry].d_table;
+    ap.out = out;
+    ap.n = n;
+    ap.H = h->H;
+    ap.C = h->C;
+    ap.T = h->T;
+    ap.Cpad = h->Cpad;
+    ap.masked = (h->occupancy[layer] < h->C) ? 1 : 0;
+    const int32_t* g = h->grp.data() + static_cast<size_t>(layer) * h->C;
+    for (int t = 0; t < h->T && t < 256; ++t) {
+        const int s0 = t * kTileSlots, s1 = std::min(s0 + kTileSlots, h->C);
+        bool occ = true;
+        for (int q = s0; q < s1 && occ; ++q) occ = (g[q] >= 0);
+        if (occ) ap.uniform[t >> 6] |= 1ull << (t & 63);
+    }
+    ap.sm_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+    ap.status = h->d_status;
+    ap.wait_ns = h->wait_ns;
+    if (launch_bf16_attention(ap, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
+    h->launches += 1;
+    h->last_stream = s;
+    return RC_OK;
+}
+
 static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out, int n, void* stream,
                          bool readtime) {
     if (!h || !Q_bf16 || !out) return RC_ERR_ARG;
@@ -596,6 +646,7 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
     if (h->last_n[layer] == 0 || n != h->last_n[layer] || h->occupancy[layer] == 0) return RC_ERR_STATE;
     if (readtime && !h->ablation) return RC_ERR_STATE;
     if (launch_fault()) return RC_ERR_CUDA;
+    if (h->bf16) return attend_bf16(h, layer, Q_bf16, out, n, stream);
     if (check_sticky() != RC_OK) return RC_ERR_CUDA;
     if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -752,9 +803,45 @@ static int export_ring(rc_cache* h, const uint8_t* d_kc, const uint8_t* d_vt, co
     return RC_OK;
 }
 
+int rc_cache_export_bf16(rc_cache* h, int layer, uint16_t* kbits, uint16_t* vbits, int64_t* pos, int64_t* gid) {
+    if (!h || layer < 0 || layer >= h->L) return RC_ERR_ARG;
+    if (!h->bf16) return RC_ERR_STATE;
+    int st = rc_cache_sync(h);
+    if (st != RC_OK) return st;
+    const int H = h->H, D = h->D, C = h->C, T = h->T;
+    const size_t tile = static_cast<size_t>(kTileSlots) * D * 2;
+    const size_t one = static_cast<size_t>(H) * T * tile;
+    const size_t lring = static_cast<size_t>(layer) * one;
+    std::vector<uint8_t> buf(one);
+    if (kbits) {
+        if (cudaMemcpy(buf.data(), h->d_kc + lring, one, cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            for (int sl = 0; sl < C; ++sl) {
+                const uint8_t* t = buf.data() + (static_cast<size_t>(hh) * T + sl / kTileSlots) * tile;
+                for (int d = 0; d < D; ++d)
+                    std::memcpy(kbits + (static_cast<size_t>(hh) * C + sl) * D + d, t + bktile_off(sl % kTileSlots, d), 2);
+            }
+    }
+    if (vbits) {
+        if (cudaMemcpy(buf.data(), h->d_vt + lring, one, cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+        for (int hh = 0; hh < H; ++hh)
+            for (int sl = 0; sl < C; ++sl) {
+                const uint8_t* t = buf.data() + (static_cast<size_t>(hh) * T + sl / kTileSlots) * tile;
+                for (int d = 0; d < D; ++d)
+                    std::memcpy(vbits + (static_cast<size_t>(hh) * C + sl) * D + d, t + bvtile_off(d, sl % kTileSlots, D),
+                                2);
+            }
+    }
+    const size_t lb = static_cast<size_t>(layer) * h->C;
+    if (pos) std::memcpy(pos, h->pos.data() + lb, sizeof(int64_t) * h->C);
+    if (gid) std::memcpy(gid, h->gid.data() + lb, sizeof(int64_t) * h->C);
+    return RC_OK;
+}
+
 int rc_cache_export(rc_cache* h, int layer, uint8_t* kcodes, float* kscale, uint8_t* vcodes, float* vscale,
                     int64_t* pos, int64_t* gid) {
     if (!h || layer < 0 || layer >= h->L) return RC_ERR_ARG;
+    if (h->bf16) return RC_ERR_STATE;
     int st = rc_cache_sync(h);
     if (st != RC_OK) return st;
     const size_t lring = static_cast<size_t>(layer) * h->H * h->T * kTileSlots * h->D;

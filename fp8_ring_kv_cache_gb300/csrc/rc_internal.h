@@ -131,6 +131,10 @@ cudaError_t launch_write(const WriteParams& p, int D, cudaStream_t s);
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status);
 cudaError_t launch_readtime(const ReadtimeParams& p, int D, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, cudaStream_t s);
+// the bf16 ring (RC_F_BF16_CACHE): kc / vt hold bf16 tiles, sk / sv are unused
+cudaError_t launch_bf16_write(const WriteParams& p, int D, cudaStream_t s);
+cudaError_t launch_bf16_rotate(const RotateParams& p, int D, int layers, cudaStream_t s);
+cudaError_t launch_bf16_attention(const AttnParams& p, int D, cudaStream_t s);
 
 // Status values a kernel writes into the device status word.
 enum DeviceStatus : int {

@@ -38,4 +38,20 @@ RC_HD uint32_t vtile_off(uint32_t drow, uint32_t slot) {
 
 RC_HD int tiles_of(int C) { return (C + kTileSlots - 1) / kTileSlots; }
 
+// The bf16 ring (RC_F_BF16_CACHE) keeps 2-byte elements in the same 128-slot
+// tiles, each a K-major tcgen05 operand image with the 128-byte swizzle:
+//   K tile  : [D/64 blocks][128 slots][128 B]: element (slot, dim) in block
+//             dim / 64, 16-byte chunk ((dim % 64) / 8) ^ (slot % 8);
+//   Vt tile : [2 halves][D dims][128 B]: element (dim, slot) in half slot / 64,
+//             16-byte chunk ((slot % 64) / 8) ^ (dim % 8).
+RC_HD uint32_t bktile_off(uint32_t slot, uint32_t dim) {
+    const uint32_t byte = (dim & 63u) * 2u;
+    return (dim >> 6) * (kTileSlots * 128u) + slot * 128u + ((((byte >> 4) ^ (slot & 7u)) << 4) | (byte & 15u));
+}
+RC_HD uint32_t bvtile_off(uint32_t drow, uint32_t slot, int D) {
+    const uint32_t byte = (slot & 63u) * 2u;
+    return (slot >> 6) * (static_cast<uint32_t>(D) * 128u) + drow * 128u +
+           ((((byte >> 4) ^ (drow & 7u)) << 4) | (byte & 15u));
+}
+
 }  // namespace rc
