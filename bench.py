@@ -42,14 +42,16 @@ ATTN_FLOP = 4.0 * N_NEW * C * D * H                      # 107.68 GFLOP per call
 WRITE_BYTES = N_NEW * H * D * (2 + 2) + N_NEW * H * D * 2  # bf16 K,V read + E4M3 K,V codes written
 ROTATE_BYTES = 2.0 * L * H * C * D                        # K codes read + written, all layers
 READTIME_EXTRA_BYTES = C * H * D * (2 + 2) + C * H * D * 2  # bf16 store read + FP8 ring written
+BF16_WRITE_BYTES = N_NEW * H * D * (2 + 2) * 2             # bf16 K,V read + bf16 K,V written
+BF16_ROTATE_BYTES = 2.0 * L * H * C * D * 2                # bf16 K read + written, all layers
 
 # dram bytes per launch measured by ncu, valid only for the kernel source they
 # were taken on
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
     # the production call, valid while rc_attention.cu has this hash
-    "attention": {"bytes": 87.45e6,
-                  "src_sha256": "7ef820408e7cef502bffe83e53b747fc8432beaaa08e81e6b12036ae76bf7fc2"},
+    "attention": {"bytes": 87.36e6,
+                  "src_sha256": "e62ad2995516cbadea3bac1e6d7be24aeeb67d49342b1db1b3c0e51d534c965f"},
 }
 
 
@@ -234,6 +236,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # ---- read-time ablation: same chunk, whole-cache RoPE + quantisation per call
     ab = run_ablation(args, dev, K, V, Q, mult, seed, kp, vp)
 
+    # ---- the same step on a bf16 ring (the FP8-versus-bf16 cache comparison)
+    peaks, peak_src = load_peaks()
+    bf = run_bf16_cache(args, dev, K, V, Q, kp, vp, peaks["bf16_tflops"])
+
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(args, dev, K, V, Q, mult, kp, vp)
 
@@ -242,7 +248,6 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     if rank != 0:
         return None
 
-    peaks, peak_src = load_peaks()
     # fp8 dense = 2x bf16 dense (nominal ratio).  The attention kernel is timed
     # per launch (microseconds, full SM clock), so the burst rate applies; the
     # fraction against the sustained (power-capped) rate is reported beside it.
@@ -299,6 +304,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                           "frac_fp8": round(achieved_tflops / fp8_peak, 4),
                           "frac_fp8_sustained": round(achieved_tflops / fp8_peak_sustained, 4)},
             "readtime_ablation": ab,
+            "bf16_cache": dict(bf, fp8_ms_per_step=round(ms_step, 4),
+                               fp8_saves_ms_per_step=round(bf["ms_per_step"] - ms_step, 4),
+                               peak_source=f"{peak_src}: bf16_tflops, the burst rate"),
             "hbm_peak_gbs": hbm, "peak_source": peak_src,
         },
         "e2e": {"value": round(job_throughput(world, args.steps, e2e_ms), 2), "unit": "calls/s",
@@ -599,6 +607,71 @@ def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
             "extra_bytes_per_call": READTIME_EXTRA_BYTES}
 
 
+def run_bf16_cache(args, dev, K, V, Q, kp, vp, bf16_peak: float) -> dict:
+    """The same step (chunk + 60-layer delta rotation) on a bf16 ring: the
+    non-FP8 side of the FP8-versus-bf16 cache comparison.  Same inputs, per-
+    kernel events on the launching stream."""
+    import numpy as np
+    import torch
+
+    import fp8_ring_kv_cache_gb300 as rc
+
+    cache = rc.RingKVCache(L, H, D, C, max_write=C, bf16_cache=True)
+    for layer in range(L):
+        cache.write(layer, kp, vp, np.arange(0, PREFILL))
+    out = torch.empty(N_NEW, H, D, dtype=torch.float32, device=dev)
+    pos = np.arange(PREFILL, PREFILL + N_NEW)
+    stream = torch.cuda.current_stream()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+
+    def step(rec=None):
+        for pas in range(PASSES):
+            for layer in range(L):
+                if rec is not None:
+                    w, a = mk(), mk()
+                    rec["w"].append(w)
+                    rec["a"].append(a)
+                    w[0].record(stream)
+                cache.write(layer, K[pas, layer], V[pas, layer], pos)
+                if rec is not None:
+                    w[1].record(stream)
+                    a[0].record(stream)
+                cache.attend(layer, Q[pas, layer], out)
+                if rec is not None:
+                    a[1].record(stream)
+        if rec is not None:
+            r = mk()
+            rec["r"].append(r)
+            r[0].record(stream)
+        cache.delta_rotate(-N_NEW)
+        if rec is not None:
+            r[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, args.steps // 2)
+    rec = {"w": [], "a": [], "r": []}
+    t0, t1 = mk()
+    t0.record(stream)
+    for _ in range(steps):
+        step(rec)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    cache.sync()
+    cache.close()
+    mean_us = lambda evs: statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3  # noqa: E731
+    w_us, a_us, r_us = mean_us(rec["w"]), mean_us(rec["a"]), mean_us(rec["r"])
+    tflops = ATTN_FLOP / (a_us * 1e-6) / 1e12
+    return {"ms_per_step": round(t0.elapsed_time(t1) / steps, 4), "steps": steps,
+            "write_us": round(w_us, 3), "write_gbs": round(BF16_WRITE_BYTES / (w_us * 1e-6) / 1e9, 1),
+            "attention_us": round(a_us, 3), "attention_tflops": round(tflops, 1),
+            "attention_frac_bf16": round(tflops / bf16_peak, 4),
+            "delta_rotate_us": round(r_us, 3),
+            "delta_rotate_gbs": round(BF16_ROTATE_BYTES / (r_us * 1e-6) / 1e9, 1),
+            "ring_bytes": 2 * L * H * C * D * 2}
+
+
 def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
     """The same step as the device-timed one (a 240-call chunk, then the
     60-layer delta rotation that restarts the window) through the public API
@@ -738,6 +811,7 @@ def run_profile_case(kind: str) -> None:
                 3 attention calls alternate between the layers.
     write     : 3 writes of 757 tokens into 3 layers.
     rotate    : 2 delta rotations of 4 full layers.
+    attention_bf16 : the attention case on a bf16 ring.
     """
     import numpy as np
     import torch
@@ -745,8 +819,10 @@ def run_profile_case(kind: str) -> None:
     import fp8_ring_kv_cache_gb300 as rc
     import synth_inputs as si
 
+    bf16 = kind == "attention_bf16"
+    kind = "attention" if bf16 else kind
     nl = {"attention": 2, "write": 3, "rotate": 4}[kind]
-    cache = rc.RingKVCache(nl, H, D, C, max_write=C)
+    cache = rc.RingKVCache(nl, H, D, C, max_write=C, bf16_cache=bf16)
     mult = si.outlier_mask(H, D, 11)
     kp = si.normal_bf16(PREFILL, H, D, 1, "cuda", mult)
     vp = si.normal_bf16(PREFILL, H, D, 2, "cuda", mult)
@@ -773,7 +849,7 @@ def run_profile_case(kind: str) -> None:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["attention", "write", "rotate"], default=None,
+    ap.add_argument("--profile", choices=["attention", "write", "rotate", "attention_bf16"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

@@ -803,6 +803,32 @@ static int export_ring(rc_cache* h, const uint8_t* d_kc, const uint8_t* d_vt, co
     return RC_OK;
 }
 
+// The stored fp16 value as bf16 bits, rounded to nearest even (exact for every
+// value that came from a bf16 input inside fp16's range).
+static uint16_t f16_to_bf16_bits(uint16_t h) {
+    const uint32_t sign = static_cast<uint32_t>(h & 0x8000u) << 16;
+    const uint32_t e = (h >> 10) & 0x1Fu, m = h & 0x3FFu;
+    uint32_t f;
+    if (e == 0x1Fu) {
+        f = sign | 0x7F800000u | (m << 13);
+    } else if (e != 0) {
+        f = sign | ((e + 112u) << 23) | (m << 13);
+    } else if (m == 0) {
+        f = sign;
+    } else {  // subnormal: m * 2^-24
+        int sh = 0;
+        uint32_t mm = m;
+        while ((mm & 0x400u) == 0) {
+            mm <<= 1;
+            ++sh;
+        }
+        f = sign | (static_cast<uint32_t>(113 - sh) << 23) | ((mm & 0x3FFu) << 13);
+    }
+    const uint32_t lsb = (f >> 16) & 1u;
+    if ((f & 0x7F800000u) == 0x7F800000u) return static_cast<uint16_t>(f >> 16);
+    return static_cast<uint16_t>((f + 0x7FFFu + lsb) >> 16);
+}
+
 int rc_cache_export_bf16(rc_cache* h, int layer, uint16_t* kbits, uint16_t* vbits, int64_t* pos, int64_t* gid) {
     if (!h || layer < 0 || layer >= h->L) return RC_ERR_ARG;
     if (!h->bf16) return RC_ERR_STATE;
@@ -827,9 +853,11 @@ int rc_cache_export_bf16(rc_cache* h, int layer, uint16_t* kbits, uint16_t* vbit
         for (int hh = 0; hh < H; ++hh)
             for (int sl = 0; sl < C; ++sl) {
                 const uint8_t* t = buf.data() + (static_cast<size_t>(hh) * T + sl / kTileSlots) * tile;
-                for (int d = 0; d < D; ++d)
-                    std::memcpy(vbits + (static_cast<size_t>(hh) * C + sl) * D + d, t + bvtile_off(d, sl % kTileSlots, D),
-                                2);
+                for (int d = 0; d < D; ++d) {
+                    uint16_t f16;
+                    std::memcpy(&f16, t + bvtile_off(d, sl % kTileSlots, D), 2);
+                    vbits[(static_cast<size_t>(hh) * C + sl) * D + d] = f16_to_bf16_bits(f16);
+                }
             }
     }
     const size_t lb = static_cast<size_t>(layer) * h->C;

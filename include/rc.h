@@ -65,14 +65,16 @@ extern "C" {
    stored tokens the way a concatenating cache would (the copy-based window
    ablation; doubles the ring memory; not combinable with the flag above). */
 #define RC_F_COPY_WINDOW 2u
-/* Store K and V as bf16 instead of E4M3 + per-slot scales: the non-FP8 cache of
-   the comparison in the cpdf.ai blog, section "Blackwell, escalabilidade e
+/* A 16-bit ring instead of E4M3 + per-slot scales: the non-FP8 cache of the
+   comparison in the cpdf.ai blog, section "Blackwell, escalabilidade e
    limites do decodificador" (FP8 saves time on H100 and costs time on B200
-   without an FP8 attention kernel).  Writes round RoPE(K) once to bf16 and copy V; delta
-   rotations re-rotate every stored key and round it back to bf16; attention reads
-   bf16 (softmax(Q K^T / sqrt(d)) V with fp32 accumulation).  Doubles the ring
-   memory, keeps no scales; rc_cache_export_bf16 replaces rc_cache_export.  Not
-   combinable with the two flags above. */
+   without an FP8 attention kernel).  Writes round RoPE(K) once to bf16 and
+   store V converted once to fp16 (exact for 2^-17 <= |v| < 65520 and zero;
+   smaller magnitudes round to fp16's subnormal step, larger ones become
+   +-inf); delta rotations re-rotate every stored key and round it back to
+   bf16; attention computes softmax(Q K^T / sqrt(d)) V with fp32 accumulation.
+   Doubles the ring memory, keeps no scales; rc_cache_export_bf16 replaces
+   rc_cache_export.  Not combinable with the two flags above. */
 #define RC_F_BF16_CACHE 4u
 
 typedef struct rc_config {
@@ -225,7 +227,8 @@ int rc_cache_export_readtime(rc_cache *h, uint8_t *kcodes, float *kscale,
 /*
  * Copy ring `layer` of a RC_F_BF16_CACHE cache to HOST buffers (synchronous):
  * kbits, vbits: uint16 [heads][slots][head_dim] bf16 bit patterns (RoPE'd keys
- * at their current positions, values as written; zeros in empty slots); pos,
+ * at their current positions; the stored fp16 values rounded to bf16, which
+ * returns each in-range value as written; zeros in empty slots); pos,
  * gid as in rc_cache_export.  Any pointer may be NULL.  RC_ERR_STATE without
  * the flag (and rc_cache_export answers RC_ERR_STATE with it).
  */

@@ -6,7 +6,10 @@ and oracle.OracleBf16Cache are driven in lockstep from the same seeded inputs;
 neither sees the other's state.
 
   positions, write serials                   : bit-exact
-  V bits                                     : bit-exact (stored as given)
+  V bits                                     : bit-exact with the oracle's V
+                                               rounded to fp16 (the ring stores
+                                               V in fp16; exact for every
+                                               2^-17 <= |v| < 65520)
   K bits                                     : >= 99.9 % identical; each of the
                                                rest within one bf16 step of the
                                                oracle plus 2^-21 of its RoPE
@@ -30,7 +33,8 @@ pair's norm.
 
 The attention bar follows from the kernel's arithmetic: the queries keep ~16
 significant bits (two bf16 pieces), the scores accumulate in fp32, P is rounded
-to fp16 (relative error <= 2^-12) and V converts exactly to fp16; O divides
+to fp16 (relative error <= 2^-12) and V is held in fp16 (exact but for
+|v| < 2^-17, off by < 2^-25 there); O divides
 sum_i p~_i v_i by l = sum_i p_i, so its error is at most 2^-12 of the largest
 |v| in the channel, plus the far smaller effects of the query's residual bits
 and of the rare key differences.  The bar takes twice that, plus 1e-3.
@@ -67,6 +71,12 @@ def bf16_step(x: np.ndarray) -> np.ndarray:
     m = np.abs(x)
     e = np.floor(np.log2(np.where(m > 0, m, 1.0)))
     return np.where(m >= 2.0 ** -126, np.exp2(e - 7), 2.0 ** -133)
+
+
+def as_f16_bits(vbits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns rounded to fp16 and returned as bf16 bit patterns."""
+    t = torch.from_numpy(vbits.astype(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float16).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 def check_keys(got: np.ndarray, want: np.ndarray, deltas: int, what: str) -> dict:
@@ -117,7 +127,7 @@ class Pair:
         assert np.array_equal(got["pos"], want["pos"]), f"{what}: positions differ"
         assert np.array_equal(got["gid"], want["gid"]), f"{what}: write serials differ"
         occ = want["pos"] != oracle.EMPTY
-        assert np.array_equal(got["vbits"][:, occ], want["vbits"][:, occ]), f"{what}: V bits differ"
+        assert np.array_equal(got["vbits"][:, occ], as_f16_bits(want["vbits"][:, occ])), f"{what}: V bits differ"
         return check_keys(got["kbits"][:, occ], want["kbits"][:, occ], self.deltas, f"{what} K bits")
 
     def attend_check(self, layer, Q, what="attention"):
@@ -210,7 +220,7 @@ def test_bf16_production_call_sampled_heads(rc, seed):
     o.write(0, t["k_new"][:, heads].cpu(), t["v_new"][:, heads].cpu(), np.arange(si.PROD_PREFILL, C))
     st = g.export(0)
     want = o.export(0)
-    assert np.array_equal(st["vbits"][heads], want["vbits"])
+    assert np.array_equal(st["vbits"][heads], as_f16_bits(want["vbits"]))
     check_keys(st["kbits"][heads], want["kbits"], 0, "production K bits")
     res = check_out(out[:, heads].cpu().numpy(), o.attend(0, t["q"][:, heads].cpu()), want["vbits"],
                     "production attention")
