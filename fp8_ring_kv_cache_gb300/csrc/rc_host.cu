@@ -84,6 +84,7 @@ struct rc_cache {
     std::vector<std::array<uint8_t, 256>> split;   // per layer: two-run tiles (first slot of the second run)
     std::vector<char> uniform_dirty;
     std::vector<uint32_t> slot_mark;
+    std::vector<int32_t> wslot;            // [max_write] slots of the write in progress
     uint32_t mark = 0;
     std::vector<double> theta;
     int64_t delta_total = 0, next_gid = 0, launches = 0;
@@ -412,6 +413,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     h->split.assign(h->L, std::array<uint8_t, 256>{});
     h->uniform_dirty.assign(h->L, 1);
     h->slot_mark.assign(h->C, 0);
+    h->wslot.assign(h->max_write, 0);
     *out = h;
     return RC_OK;
 }
@@ -430,15 +432,28 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
     if (launch_fault()) return RC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // distinct slots
-    if (++h->mark == 0) {
-        std::fill(h->slot_mark.begin(), h->slot_mark.end(), 0u);
-        h->mark = 1;
-    }
-    for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
-        if (h->slot_mark[slot] == h->mark) return RC_ERR_ARG;
-        h->slot_mark[slot] = h->mark;
+    // the tokens' slots: an arithmetic run (the usual write) takes one modulo
+    // and its n <= C slots are distinct; any other run is checked slot by slot
+    int32_t* sl = h->wslot.data();
+    bool arith = true;
+    for (int t = 1; t < n && arith; ++t) arith = positions[t] == positions[0] + t;
+    if (arith) {
+        int32_t s0 = static_cast<int32_t>(floormod(positions[0] - h->delta_total - h->slot_shift, h->C));
+        for (int t = 0; t < n; ++t) {
+            sl[t] = s0;
+            if (++s0 == h->C) s0 = 0;
+        }
+    } else {
+        if (++h->mark == 0) {
+            std::fill(h->slot_mark.begin(), h->slot_mark.end(), 0u);
+            h->mark = 1;
+        }
+        for (int t = 0; t < n; ++t) {
+            const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
+            if (h->slot_mark[slot] == h->mark) return RC_ERR_ARG;
+            h->slot_mark[slot] = h->mark;
+            sl[t] = static_cast<int32_t>(slot);
+        }
     }
     if (check_sticky() != RC_OK) return RC_ERR_CUDA;
     if (cudaSetDevice(h->device) != cudaSuccess) return RC_ERR_CUDA;
@@ -452,7 +467,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     auto& rc = h->refcnt[layer];
     auto& fl = h->freelist[layer];
     for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
+        const int32_t slot = sl[t];
         const int32_t old = h->grp[lb + slot];
         if (old >= 0) {
             if (--rc[old] == 0) fl.push_back(old);
@@ -464,7 +479,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     fl.pop_back();
     rc[g] = n;
     for (int t = 0; t < n; ++t) {
-        const int64_t slot = floormod(positions[t] - h->delta_total - h->slot_shift, h->C);
+        const int32_t slot = sl[t];
         h->pos[lb + slot] = positions[t];
         h->gid[lb + slot] = h->next_gid;
         h->grp[lb + slot] = g;
@@ -484,7 +499,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     wp.pos = re.arith ? nullptr : re.d_pos;
     wp.p0 = positions[0];
     wp.delta_total = h->delta_total + h->slot_shift;  // the kernel's slot mapping
-    wp.slot0 = static_cast<int>(floormod(positions[0] - h->delta_total - h->slot_shift, h->C));
+    wp.slot0 = sl[0];
     wp.status = h->d_status;
     wp.n = n;
     wp.H = h->H;
