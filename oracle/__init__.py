@@ -79,6 +79,8 @@ def _load():
         lib.orc_slot_of.restype = i64
         lib.orc_write.argtypes = [P, i32, P, P, P, i32]
         lib.orc_write.restype = i32
+        lib.orc_write_proj.argtypes = [P, i32, P, f64, P, f64, P, f64, i32, P, i32]
+        lib.orc_write_proj.restype = i32
         lib.orc_delta_rotate.argtypes = [P, i64]
         lib.orc_delta_rotate.restype = None
         lib.orc_attend.argtypes = [P, i32, P, i32, P]
@@ -125,6 +127,14 @@ def _load():
 def _ptr(a: np.ndarray):
     assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(x) -> np.ndarray:
+    """uint8 codes as a contiguous numpy array (accepts a torch uint8 tensor or a numpy array)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint8
+        return np.ascontiguousarray(x)
+    return np.ascontiguousarray(x.detach().cpu().contiguous().numpy())
 
 
 def _bf16_bits(x) -> np.ndarray:
@@ -254,6 +264,19 @@ class OracleCache:
         n = pos.shape[0]
         assert kb.shape == (n, self.H, self.d) and vb.shape == kb.shape
         rc = self._lib.orc_write(self._h, layer, _ptr(kb), _ptr(vb), _ptr(pos), n)
+        if rc != 0:
+            raise ValueError("oracle write rejected (layer, n or duplicate slot)")
+
+    def write_proj(self, layer: int, X, xs: float, Wk, wks: float, Wv, wvs: float, positions) -> None:
+        """The write fused into the K/V projection: X [n][hidden], Wk and Wv
+        [H*d][hidden] uint8 E4M3 codes with one scale each (see orc_write_proj)."""
+        x = _u8(X)
+        wk, wv = _u8(Wk), _u8(Wv)
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        n, hidden = x.shape
+        assert n == pos.shape[0] and wk.shape == (self.H * self.d, hidden) and wv.shape == wk.shape
+        rc = self._lib.orc_write_proj(self._h, layer, _ptr(x), float(xs), _ptr(wk), float(wks), _ptr(wv),
+                                      float(wvs), hidden, _ptr(pos), n)
         if rc != 0:
             raise ValueError("oracle write rejected (layer, n or duplicate slot)")
 

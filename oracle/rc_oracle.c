@@ -264,12 +264,12 @@ static float quantise_group(const double *x, size_t rows, int d, uint8_t *codes)
 }
 
 /*
- * Write n new tokens to layer l.  K, V are bf16 bit patterns [n][H][d];
+ * The write proper, from fp64 rows: K, V [n][H][d] (values, not yet rotated);
  * positions[n].  Returns 0, or -1 on bad arguments (n out of range, layer out
  * of range, two tokens on one slot).
  */
-int orc_write(orc_cache *c, int l, const uint16_t *K, const uint16_t *V,
-              const int64_t *positions, int n)
+static int write_rows(orc_cache *c, int l, const double *K, const double *V,
+                      const int64_t *positions, int n)
 {
     if (!c || l < 0 || l >= c->L || n <= 0 || n > c->C)
         return -1;
@@ -293,8 +293,8 @@ int orc_write(orc_cache *c, int l, const uint16_t *K, const uint16_t *V,
         for (int t = 0; t < n; ++t)
             for (int i = 0; i < d; ++i) {
                 size_t src = ((size_t)t * H + h) * d + i;
-                xk[(size_t)t * d + i] = orc_bf16_to_double(K[src]);
-                xv[(size_t)t * d + i] = orc_bf16_to_double(V[src]);
+                xk[(size_t)t * d + i] = K[src];
+                xv[(size_t)t * d + i] = V[src];
             }
         orc_rope_rows(xk, n, d, positions, c->base);
         float sk = quantise_group(xk, (size_t)n, d, ck);
@@ -315,6 +315,71 @@ int orc_write(orc_cache *c, int l, const uint16_t *K, const uint16_t *V,
     c->next_gid += 1;
     free(xk); free(xv); free(ck); free(cv); free(slot);
     return 0;
+}
+
+/*
+ * Write n new tokens to layer l.  K, V are bf16 bit patterns [n][H][d];
+ * positions[n].  Returns 0, or -1 on bad arguments.
+ */
+int orc_write(orc_cache *c, int l, const uint16_t *K, const uint16_t *V,
+              const int64_t *positions, int n)
+{
+    if (!c || n <= 0 || n > c->C)
+        return -1;
+    size_t m = (size_t)n * c->H * c->d;
+    double *k = (double *)malloc(sizeof(double) * m);
+    double *v = (double *)malloc(sizeof(double) * m);
+    for (size_t i = 0; i < m; ++i) {
+        k[i] = orc_bf16_to_double(K[i]);
+        v[i] = orc_bf16_to_double(V[i]);
+    }
+    int r = write_rows(c, l, k, v, positions, n);
+    free(k); free(v);
+    return r;
+}
+
+/*
+ * The write fused into the K/V projection (the single-GPU half of the pages'
+ * fused FP8 GEMM; paperdot abstract and cpdf.ai blog): X [n][hidden],
+ * Wk and Wv [H*d][hidden] are E4M3 codes with one scale each, and
+ *   K[t][h][i] = xs * wks * sum_k X[t][k] Wk[h*d + i][k]
+ * (V alike with Wv, wvs) is the exact product of the decoded operands (a sum
+ * of at most 2^13 products of two E4M3 values needs fewer than 53 bits, so
+ * fp64 holds it exactly).  Those fp64 rows are then written as orc_write
+ * writes its inputs: no bf16 rounding in between.
+ */
+int orc_write_proj(orc_cache *c, int l, const uint8_t *X, double xs, const uint8_t *Wk, double wks,
+                   const uint8_t *Wv, double wvs, int hidden, const int64_t *positions, int n)
+{
+    if (!c || n <= 0 || n > c->C || hidden <= 0)
+        return -1;
+    int F = c->H * c->d;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)n * hidden);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)F * hidden);
+    double *wv = (double *)malloc(sizeof(double) * (size_t)F * hidden);
+    for (size_t i = 0; i < (size_t)n * hidden; ++i) xd[i] = orc_e4m3_decode(X[i]);
+    for (size_t i = 0; i < (size_t)F * hidden; ++i) {
+        wk[i] = orc_e4m3_decode(Wk[i]);
+        wv[i] = orc_e4m3_decode(Wv[i]);
+    }
+    double *k = (double *)malloc(sizeof(double) * (size_t)n * F);
+    double *v = (double *)malloc(sizeof(double) * (size_t)n * F);
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < n; ++t)
+        for (int f = 0; f < F; ++f) {
+            const double *xr = xd + (size_t)t * hidden;
+            const double *kr = wk + (size_t)f * hidden, *vr = wv + (size_t)f * hidden;
+            double sk = 0.0, sv = 0.0;
+            for (int q = 0; q < hidden; ++q) {
+                sk += xr[q] * kr[q];
+                sv += xr[q] * vr[q];
+            }
+            k[(size_t)t * F + f] = sk * xs * wks;
+            v[(size_t)t * F + f] = sv * xs * wvs;
+        }
+    int r = write_rows(c, l, k, v, positions, n);
+    free(xd); free(wk); free(wv); free(k); free(v);
+    return r;
 }
 
 /*
