@@ -25,7 +25,7 @@ from ._binding import (  # noqa: F401
     RC_F_BF16_CACHE, RC_F_COPY_WINDOW, RC_F_READTIME_ABLATION, RC_OK, RcError, RingKVCache, declared_symbols, lib, rc_attend, rc_attend_readtime,
     rc_cache_create, rc_cache_delta_rotate, rc_cache_delta_total, rc_cache_destroy, rc_cache_export,
     rc_cache_export_bf16, rc_cache_export_readtime, rc_cache_launch_count, rc_cache_occupancy, rc_cache_set_wait_limit, rc_cache_sync,
-    rc_cache_write,
+    rc_cache_write, rc_cache_write_fused,
     rc_cache_window_shift, rc_tile_kinds,
     rc_status_string,
 )

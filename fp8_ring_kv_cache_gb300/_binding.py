@@ -66,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_export": ([P, I, P, P, P, P, P, P], I),
         "rc_cache_export_readtime": ([P, P, P, P, P], I),
         "rc_cache_export_bf16": ([P, I, P, P, P, P], I),
+        "rc_cache_write_fused": ([P, I, P, ctypes.c_float, P, ctypes.c_float, P, ctypes.c_float, I, P, I, P], I),
         "rc_cache_occupancy": ([P, I], I),
         "rc_cache_delta_total": ([P], I64),
         "rc_cache_launch_count": ([P], I64),
@@ -143,6 +144,20 @@ def rc_cache_write(h, layer: int, K, V, positions, heads: int, head_dim: int, st
     vp = _dev_ptr(V, torch.bfloat16, shape, "V")
     _check(lib.rc_cache_write(h, int(layer), kp, vp, pos.ctypes.data_as(ctypes.c_void_p), n, _stream_ptr(stream)),
            "rc_cache_write")
+
+
+def rc_cache_write_fused(h, layer: int, X, x_scale: float, Wk, wk_scale: float, Wv, wv_scale: float, positions,
+                         heads: int, head_dim: int, stream=None) -> None:
+    """X: CUDA uint8 [n][hidden] E4M3 codes; Wk, Wv: CUDA uint8 [heads*head_dim][hidden]."""
+    import torch
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    n = pos.shape[0]
+    hidden = X.shape[1]
+    xp = _dev_ptr(X, torch.uint8, (n, hidden), "X")
+    kp = _dev_ptr(Wk, torch.uint8, (heads * head_dim, hidden), "Wk")
+    vp = _dev_ptr(Wv, torch.uint8, (heads * head_dim, hidden), "Wv")
+    _check(lib.rc_cache_write_fused(h, int(layer), xp, float(x_scale), kp, float(wk_scale), vp, float(wv_scale),
+                                    int(hidden), _np_ptr(pos), n, _stream_ptr(stream)), "rc_cache_write_fused")
 
 
 def rc_cache_delta_rotate(h, delta: int, stream=None) -> None:
@@ -254,6 +269,10 @@ class RingKVCache:
 
     def write(self, layer, K, V, positions, stream=None):
         rc_cache_write(self.handle, layer, K, V, positions, self.heads, self.head_dim, stream)
+
+    def write_fused(self, layer, X, x_scale, Wk, wk_scale, Wv, wv_scale, positions, stream=None):
+        rc_cache_write_fused(self.handle, layer, X, x_scale, Wk, wk_scale, Wv, wv_scale, positions, self.heads,
+                             self.head_dim, stream)
 
     def delta_rotate(self, delta, stream=None):
         rc_cache_delta_rotate(self.handle, delta, stream)

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librc.so")
 SOURCES = ["rc_host.cu", "rc_write.cu", "rc_rotate.cu", "rc_attention.cu", "rc_noalloc.cu", "rc_window.cu",
-           "rc_bf16.cu"]
+           "rc_bf16.cu", "rc_fused.cu"]
 HEADERS = ["rc_device.cuh", "rc_internal.h", "rc_layout.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

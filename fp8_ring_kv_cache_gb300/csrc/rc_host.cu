@@ -425,13 +425,12 @@ void rc_cache_destroy(rc_cache* h) {
     free_all(h);
 }
 
-int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf16, const int64_t* positions, int n,
-                   void* stream) {
-    if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
-    if (!aligned16(K_bf16) || !aligned16(V_bf16)) return RC_ERR_ARG;
-    if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
-    if (launch_fault()) return RC_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The bookkeeping of a write (slots, RoPE table, write groups) around the
+// launch of its kernel: `launch` gets the filled WriteParams (inputs left
+// for it to set) and launches on stream s.
+extern "C++" {
+template <typename Launch>
+static int write_common(rc_cache* h, int layer, const int64_t* positions, int n, cudaStream_t s, Launch&& launch) {
     // the tokens' slots: an arithmetic run (the usual write) takes one modulo
     // and its n <= C slots are distinct; any other run is checked slot by slot
     int32_t* sl = h->wslot.data();
@@ -493,8 +492,6 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     wp.sk = h->bf16 ? nullptr : h->d_sk + lsc;
     wp.sv = h->bf16 ? nullptr : h->d_sv + lsc;
     wp.grp = h->d_grp + static_cast<size_t>(layer) * h->Cpad;
-    wp.K = static_cast<const __nv_bfloat16*>(K_bf16);
-    wp.V = static_cast<const __nv_bfloat16*>(V_bf16);
     wp.rope = re.d_table;
     wp.pos = re.arith ? nullptr : re.d_pos;
     wp.p0 = positions[0];
@@ -513,7 +510,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
         wp.vraw = h->d_vraw + raw;
         wp.slot_pos = h->d_slot_pos + static_cast<size_t>(layer) * h->Cpad;
     }
-    if ((h->bf16 ? launch_bf16_write(wp, h->D, s) : launch_write(wp, h->D, s)) != cudaSuccess) return RC_ERR_CUDA;
+    if (launch(wp) != cudaSuccess) return RC_ERR_CUDA;
     h->launches += 1;
     h->last_pos[layer].assign(positions, positions + n);
     h->uniform_dirty[layer] = 1;
@@ -522,6 +519,44 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
     h->next_gid += 1;
     h->last_stream = s;
     return RC_OK;
+}
+
+}  // extern "C++"
+
+int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf16, const int64_t* positions, int n,
+                   void* stream) {
+    if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
+    if (!aligned16(K_bf16) || !aligned16(V_bf16)) return RC_ERR_ARG;
+    if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
+    if (launch_fault()) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return write_common(h, layer, positions, n, s, [&](WriteParams& wp) {
+        wp.K = static_cast<const __nv_bfloat16*>(K_bf16);
+        wp.V = static_cast<const __nv_bfloat16*>(V_bf16);
+        return h->bf16 ? launch_bf16_write(wp, h->D, s) : launch_write(wp, h->D, s);
+    });
+}
+
+int rc_cache_write_fused(rc_cache* h, int layer, const uint8_t* X, float x_scale, const uint8_t* Wk, float wk_scale,
+                         const uint8_t* Wv, float wv_scale, int hidden, const int64_t* positions, int n,
+                         void* stream) {
+    if (!h || !X || !Wk || !Wv || !positions) return RC_ERR_ARG;
+    if (!aligned16(X) || !aligned16(Wk) || !aligned16(Wv)) return RC_ERR_ARG;
+    if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write || n > kFusedMaxTokens) return RC_ERR_ARG;
+    if (hidden < 64 || hidden % 64 != 0) return RC_ERR_ARG;
+    if (!(x_scale > 0.f) || !(wk_scale > 0.f) || !(wv_scale > 0.f)) return RC_ERR_ARG;
+    if (h->bf16 || h->ablation) return RC_ERR_UNSUPPORTED;
+    if (launch_fault()) return RC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return write_common(h, layer, positions, n, s, [&](WriteParams& wp) {
+        FusedParams fp{};
+        fp.w = wp;
+        fp.k_mul = x_scale * wk_scale;
+        fp.v_mul = x_scale * wv_scale;
+        fp.hidden = hidden;
+        fp.wait_ns = h->wait_ns;
+        return launch_fused_write(fp, X, Wk, Wv, h->D, s);
+    });
 }
 
 int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {

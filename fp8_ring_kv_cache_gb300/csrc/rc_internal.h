@@ -58,6 +58,18 @@ struct WriteParams {
     int* status;           // device status word (bounded waits)
 };
 
+// K2f: the write fused into the K/V projection: K = k_mul X Wk^T,
+// V = v_mul X Wv^T on the tensor cores, then the write of K2 from the fp32
+// accumulators.  Uses w's ring, scale, group, RoPE and slot fields (w.K and
+// w.V are unused).
+constexpr int kFusedMaxTokens = 2048;  // 8 blocks of 256 rows: one cluster along M
+struct FusedParams {
+    WriteParams w;
+    float k_mul, v_mul;  // x_scale * wk_scale, x_scale * wv_scale
+    int hidden;          // projection input width (a multiple of 64)
+    uint64_t wait_ns;    // bound of one device wait
+};
+
 // K3: in-place delta rotation with per-(layer, head, group) requantisation.
 struct RotateParams {
     uint8_t* kc;           // all layers [L][H][T][128][D]
@@ -135,6 +147,9 @@ cudaError_t launch_attention(const AttnParams& p, int D, cudaStream_t s);
 cudaError_t launch_bf16_write(const WriteParams& p, int D, cudaStream_t s);
 cudaError_t launch_bf16_rotate(const RotateParams& p, int D, int layers, cudaStream_t s);
 cudaError_t launch_bf16_attention(const AttnParams& p, int D, cudaStream_t s);
+// the fused projection + write: X [n][hidden], Wk / Wv [H*D][hidden] E4M3 codes
+cudaError_t launch_fused_write(const FusedParams& p, const uint8_t* X, const uint8_t* Wk, const uint8_t* Wv, int D,
+                               cudaStream_t s);
 
 // Status values a kernel writes into the device status word.
 enum DeviceStatus : int {

@@ -206,6 +206,32 @@ int rc_cache_sync(rc_cache *h);
 int rc_cache_set_wait_limit(rc_cache *h, uint64_t ns);
 
 /*
+ * Write n new tokens into ring `layer` straight from the K/V projection: the
+ * write fused into the projection's FP8 GEMM (the single-GPU half of the
+ * pages' fused FP8 GEMM: paperdot abstract; cpdf.ai blog, "Como rodar 57B em
+ * tempo real com batch size 1").  With X, Wk, Wv E4M3 codes and one scale
+ * each,
+ *   K[t][h][i] = x_scale * wk_scale * sum_k X[t][k] * Wk[h*head_dim + i][k]
+ * and V likewise with Wv, wv_scale, computed on the tensor cores (fp32
+ * accumulation); then written as rc_cache_write writes its K and V (RoPE at
+ * positions[t], one scale per head for K and for V, E4M3 codes into the
+ * slots), from the fp32 products with no bf16 rounding in between.
+ * X: device [n][hidden] uint8, row stride hidden bytes; Wk, Wv: device
+ * [heads*head_dim][hidden] uint8 (one weight row per output feature); all
+ * 16-byte aligned.  hidden: a multiple of 64.  positions: HOST int64 [n], as
+ * for rc_cache_write.  Stream-ordered; the caller keeps X, Wk, Wv alive until
+ * the work on `stream` has finished.
+ * Errors: RC_ERR_ARG (a pointer NULL or unaligned, layer out of range, n < 1,
+ * n > max_write or n > 2048, hidden not a positive multiple of 64, a scale not
+ * positive, two tokens on one slot); RC_ERR_UNSUPPORTED with RC_F_BF16_CACHE
+ * or RC_F_READTIME_ABLATION (the read-time store keeps bf16 K and V, which
+ * this path never forms).
+ */
+int rc_cache_write_fused(rc_cache *h, int layer, const uint8_t *X, float x_scale,
+                         const uint8_t *Wk, float wk_scale, const uint8_t *Wv, float wv_scale,
+                         int hidden, const int64_t *positions, int n, void *stream);
+
+/*
  * Copy ring `layer` to HOST buffers in canonical layout (synchronous):
  * kcodes, vcodes: uint8 [heads][slots][head_dim] E4M3 codes; kscale, vscale:
  * fp32 [heads][slots]; pos: int64 [slots] position (INT64_MIN = empty);

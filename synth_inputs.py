@@ -147,3 +147,24 @@ def stress_deltas(seed: int, count: int = 100, lo: int = -200000, hi: int = 0) -
     """Reset deltas drawn uniformly from the integers in [lo, hi]."""
     g = _gen(subseed(seed, 0xDE17A), "cpu")
     return [int(x) for x in torch.randint(lo, hi + 1, (count,), generator=g)]
+
+
+PROD_HIDDEN = 6144  # projection input width (48 heads x 128)
+
+
+def proj_operands(seed: int, n: int, hidden: int, features: int, device="cpu"):
+    """E4M3 operands of the K/V projection: X [n][hidden] from N(0, 1) and Wk,
+    Wv [features][hidden] from N(0, 1/hidden), each encoded with one scale
+    (amax / 448) by torch's E4M3 cast.  Returns (X, x_scale, Wk, wk_scale, Wv,
+    wv_scale), the codes as uint8 tensors on `device`."""
+    g = _gen(subseed(seed, 0x9E0), "cpu")
+
+    def enc(t: torch.Tensor):
+        s = float(t.abs().max()) / 448.0
+        codes = (t / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        return codes.to(device), s
+
+    x, xs = enc(torch.randn(n, hidden, generator=g))
+    wk, wks = enc(torch.randn(features, hidden, generator=g) / hidden ** 0.5)
+    wv, wvs = enc(torch.randn(features, hidden, generator=g) / hidden ** 0.5)
+    return x, xs, wk, wks, wv, wvs
