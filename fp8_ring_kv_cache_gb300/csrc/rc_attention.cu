@@ -872,6 +872,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     }
 
     // ------------------------------------------------------------ teardown
+    // a role's other lanes wait here for its lane 0, so every warp arrives at
+    // the CTA barrier converged
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {

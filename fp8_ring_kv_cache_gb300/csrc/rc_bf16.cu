@@ -565,6 +565,9 @@ __global__ void __launch_bounds__(kBAttnThreads, 1) bf16_attn_kernel(AttnParams 
     // warp 7 only helps prepare the queries
 
     // ------------------------------------------------------------ teardown
+    // a role's other lanes wait here for its lane 0, so every warp arrives at
+    // the CTA barrier converged
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == kBWarpMma) {

@@ -5,22 +5,25 @@
 // (RoPE, per-head amax and scale, E4M3 codes), so the bf16 K and V never go
 // to HBM and back.
 //
-// K2f fused_write_kernel: one CTA = one head x 256 rows (two M tiles of 128
-//    tokens); one thread-block cluster spans the blocks of rows of a head, so
-//    the head's amax over all n tokens is agreed through DSMEM as in K2.
-//    Warp 0 feeds the stages by TMA (tiled, 64-byte swizzle: X rows for both
-//    M tiles, then the head's Wk rows and Wv rows, which together form the
-//    N = 2 d operand), warp 1 issues tcgen05.mma kind::f8f6f4 M128 N(2d) K32
-//    into TMEM (one accumulator of 2 d columns per M tile: K columns, then V
-//    columns), warps 2..5 run the epilogue, one TMEM lane (a token) a thread:
+// K2f fused_write_kernel: one CTA = one head's K (or V) x 256 tokens (two M
+//    tiles of 128); one thread-block cluster spans the blocks of rows of that
+//    head and part (up to 8: n <= 2048), so its amax over all n tokens is
+//    agreed through DSMEM as in K2.  Two CTAs share an SM (2 d TMEM columns and
+//    96 KB of stages each) and a cluster is at most 8 CTAs, which keeps the
+//    production write (96 clusters of 3) resident in one wave; a CTA taking
+//    both K and V of a head would need clusters of 6, of which only 46 fit.
+//    Warp 0 feeds the stages by TMA (tiled, 64-byte swizzle: the two M tiles'
+//    X rows, then the head's Wk or Wv rows), warp 1 issues tcgen05.mma
+//    kind::f8f6f4 M128 N(d) K32 into TMEM (one accumulator of d columns per M
+//    tile), warps 2..5 run the epilogue, one TMEM lane (a token) a thread:
 //    pass 1 scales the accumulators (x_scale * w_scale), rotates K by RoPE at
-//    the token's position and takes the amax of K and of V; after the cluster
-//    agrees on the head's scales, pass 2 reloads the accumulators, repeats the
-//    same fp32 arithmetic and stores E4M3 codes into the ring: each token's K
-//    row as 16-byte chunks into its swizzled K-tile row, V transposed byte by
-//    byte into the Vt tile (a warp's 32 tokens write 32 consecutive slots of
-//    one dim row).  The per-element arithmetic after the product is K2's:
-//    fp32 RoPE with the write's cos/sin table, s = fl32(amax / 448), codes of
+//    the token's position and takes the amax; after the cluster agrees on the
+//    head's scale, pass 2 reloads the accumulators, repeats the same fp32
+//    arithmetic and stores E4M3 codes into the ring: each token's K row as
+//    16-byte chunks into its swizzled K-tile row, or V transposed byte by byte
+//    into the Vt tile (a warp's 32 tokens write 32 consecutive slots of one
+//    dim row).  The per-element arithmetic after the product is K2's: fp32
+//    RoPE with the write's cos/sin table, s = fl32(amax / 448), codes of
 //    fl32(x / s) by the same exact division.
 #include <atomic>
 #include <cuda.h>
@@ -44,15 +47,15 @@ enum : int { FB_FULL = 0, FB_EMPTY = kFStages, FB_DONE = 2 * kFStages, FB_DRAIN 
 template <int D>
 struct FusedLayout {
     static constexpr uint32_t kA = 128 * kFBK;                // one M tile's X rows of a stage
-    static constexpr uint32_t kB = 2 * D * kFBK;              // the head's Wk rows, then its Wv rows
-    static constexpr uint32_t kStage = 2 * kA + kB;           // 32 KB (d = 128) or 24 KB (d = 64)
+    static constexpr uint32_t kB = D * kFBK;                  // the head's Wk (or Wv) rows
+    static constexpr uint32_t kStage = 2 * kA + kB;           // 24 KB (d = 128) or 20 KB (d = 64)
     static constexpr uint32_t kBar = kFStages * kStage;
     static constexpr uint32_t kMisc = kBar + 8 * FB_COUNT;    // [0] tmem base, [1] abort flag
-    static constexpr uint32_t kRed = kMisc + 16;              // float [2][4]: the epilogue warps' maxima
-    static constexpr uint32_t kTab = kRed + 32;               // float [2][8]: the cluster's maxima
+    static constexpr uint32_t kRed = kMisc + 16;              // float [4]: the epilogue warps' maxima
+    static constexpr uint32_t kTab = kRed + 16;               // float [8]: the cluster's maxima
     static constexpr uint32_t kTotal = kTab + 64;
     static constexpr uint32_t kAlloc = kTotal + 1024;
-    static constexpr uint32_t kTmemCols = 2 * 2 * D;          // two accumulators of 2 d columns
+    static constexpr uint32_t kTmemCols = 2 * D;              // two accumulators of d columns
 };
 
 // 2-D tiled TMA load of the box at (x = reduction byte offset, y = row) into
@@ -65,7 +68,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(kFThreads, 1)
+__global__ void __launch_bounds__(kFThreads, 2)
     fused_write_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWk,
                        const __grid_constant__ CUtensorMap tmWv, FusedParams p) {
     using Lay = FusedLayout<D>;
@@ -77,11 +80,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float* tab = reinterpret_cast<float*>(smem + Lay::kTab);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y;
+    const int kv = blockIdx.z;     // 0: K, 1: V
     const int mb = blockIdx.x;     // block of 256 rows = rank in the cluster (the cluster spans blockIdx.x)
     const int nblk = gridDim.x;    // the cluster's size
     const WriteParams& w = p.w;
     const int row0 = mb * kFRows;
     const int nk = p.hidden / kFBK;
+    const CUtensorMap* tmW = kv ? &tmWv : &tmWk;
     AbortState ab{reinterpret_cast<volatile uint32_t*>(&misc[1]), w.status, p.wait_ns};
     // every CTA of the cluster is running once this barrier phase completes
     cluster_arrive_relaxed();
@@ -121,8 +126,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 // X rows past n read as zero (out-of-range boxes are filled)
                 tma_load_2d(st, &tmX, k * kFBK, row0, full);
                 tma_load_2d(st + Lay::kA, &tmX, k * kFBK, row0 + 128, full);
-                tma_load_2d(st + 2 * Lay::kA, &tmWk, k * kFBK, h * D, full);
-                tma_load_2d(st + 2 * Lay::kA + D * kFBK, &tmWv, k * kFBK, h * D, full);
+                tma_load_2d(st + 2 * Lay::kA, tmW, k * kFBK, h * D, full);
                 issued = k + 1;
             }
             if (*ab.flag) {
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     } else if (warp == kFWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(kFmtE4M3, kFmtE4M3, 128, 2 * D);
+            const uint32_t idesc = instr_desc(kFmtE4M3, kFmtE4M3, 128, D);
             // K-major operands with the 64-byte swizzle: 8-row groups 512 bytes
             // apart; a K step of 32 elements is 32 bytes along the row
             const uint64_t d0 = smem_desc(smem_u32(smem), 16, 512, 4);
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 for (int kk = 0; kk < kFBK / 32; ++kk)
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt)
-                        mma_f8_ss(tmem + mt * 2 * D, sd + ((mt * Lay::kA + kk * 32) >> 4),
+                        mma_f8_ss(tmem + mt * D, sd + ((mt * Lay::kA + kk * 32) >> 4),
                                   sd + ((2 * Lay::kA + kk * 32) >> 4), idesc, (k | kk) != 0 ? 1u : 0u);
                 mma_commit(&bars[FB_EMPTY + s]);
             }
@@ -166,6 +170,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
         }
     }
+    // the producer's and the issuer's other lanes wait here for lane 0: every
+    // warp arrives at the barriers below converged
+    __syncwarp();
 
     // ------------------------------------------------------------ epilogue
     const bool epi = warp >= kFWarpEpi0;
@@ -178,13 +185,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         return static_cast<int>(floormod64(w.pos[t] - w.delta_total, w.C));
     };
-    // columns [32c, 32c + 32) of M tile mt's K part (kv = 0) or V part (kv = 1)
-    // for token t (this thread's TMEM lane): the accumulator times its scale
-    // product, and for K rotated at the token's position (fp32, K2's cos/sin)
-    auto chunk = [&](int mt, int kv, int c, int t, float (&x)[32]) {
+    // columns [32c, 32c + 32) of M tile mt for token t (this thread's TMEM
+    // lane): the accumulator times its scale product, and for K rotated at the
+    // token's position (fp32, K2's cos/sin)
+    const float mul = kv ? p.v_mul : p.k_mul;
+    auto chunk = [&](int mt, int c, int t, float (&x)[32]) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + static_cast<uint32_t>(mt * 2 * D + kv * D + 32 * c), v);
-        const float mul = kv ? p.v_mul : p.k_mul;
+        tmem_ld32(tmem + lane_off + static_cast<uint32_t>(mt * D + 32 * c), v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = __fmul_rn(__uint_as_float(v[e]), mul);
         if (kv == 0 && t < w.n) {
@@ -201,8 +208,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     };
     bool eok = true;
     if (epi) {
-        // ---- pass 1: the amax of K (rotated) and of V over this CTA's tokens
-        float amk = 0.f, amv = 0.f;
+        // ---- pass 1: the amax over this CTA's tokens
+        float am = 0.f;
         eok = warp_wait(&bars[FB_DONE], 0, ab, kDevTimeoutEpilogue);
         if (eok) {
             tc_fence_after();
@@ -210,55 +217,36 @@ __global__ void __launch_bounds__(kFThreads, 1)
             for (int mt = 0; mt < 2; ++mt) {
                 const int t = row0 + mt * 128 + quad * 32 + lane;  // rows past n hold zeros
 #pragma unroll 1
-                for (int kv = 0; kv < 2; ++kv)
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float x[32];
-                        chunk(mt, kv, c, t, x);
-                        float m = 0.f;
+                for (int c = 0; c < D / 32; ++c) {
+                    float x[32];
+                    chunk(mt, c, t, x);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) m = max3(m, fabsf(x[e]), fabsf(x[e + 1]));
-                        if (kv == 0)
-                            amk = fmaxf(amk, m);
-                        else
-                            amv = fmaxf(amv, m);
-                    }
+                    for (int e = 0; e < 32; e += 2) am = max3(am, fabsf(x[e]), fabsf(x[e + 1]));
+                }
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            amk = fmaxf(amk, __shfl_xor_sync(0xffffffffu, amk, o));
-            amv = fmaxf(amv, __shfl_xor_sync(0xffffffffu, amv, o));
-        }
-        if (lane == 0) {
-            red[quad] = amk;
-            red[4 + quad] = amv;
-        }
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) red[quad] = am;
     }
     __syncthreads();
-    // ---- across the cluster: each CTA pushes its two maxima into every CTA's
+    // ---- across the cluster: each CTA pushes its maximum into every CTA's
     // table; one barrier makes them visible
     cluster_wait();  // (the arrival at kernel start) every CTA is running
-    if (tid < 2 * nblk) {
-        const int which = tid / nblk, r = tid % nblk;
-        const float m = fmaxf(fmaxf(red[4 * which], red[4 * which + 1]), fmaxf(red[4 * which + 2], red[4 * which + 3]));
-        dsmem_st_u32(map_shared(&tab[8 * which + mb], r), __float_as_uint(m));
+    if (tid < nblk) {
+        const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        dsmem_st_u32(map_shared(&tab[mb], tid), __float_as_uint(m));
     }
     cluster_sync();  // the pushes are visible; no CTA touches another's shared memory after this
-    float mk = 0.f, mv = 0.f;
-    for (int r = 0; r < nblk; ++r) {
-        mk = fmaxf(mk, tab[r]);
-        mv = fmaxf(mv, tab[8 + r]);
-    }
-    const float sK = (mk > 0.f) ? __fdiv_rn(mk, 448.f) : 1.f;
-    const float sV = (mv > 0.f) ? __fdiv_rn(mv, 448.f) : 1.f;
-    const float rK = __frcp_rn(sK), rV = __frcp_rn(sV);
+    float mx = 0.f;
+    for (int r = 0; r < nblk; ++r) mx = fmaxf(mx, tab[r]);
+    const float sc = (mx > 0.f) ? __fdiv_rn(mx, 448.f) : 1.f;
+    const float rc = __frcp_rn(sc);
     // fl32(x / s) by div_by_scale's three steps on packed pairs, as in K2
-    const float2 rK2 = make_float2(rK, rK), nsK2 = make_float2(-sK, -sK);
-    const float2 rV2 = make_float2(rV, rV), nsV2 = make_float2(-sV, -sV);
-    auto div2 = [](float2 x, float2 r, float2 ns) {
-        const float2 q0 = mul2(x, r);
-        return fma2(fma2(q0, ns, x), r, q0);
+    const float2 r2 = make_float2(rc, rc), ns2 = make_float2(-sc, -sc);
+    auto div2 = [&](float2 x) {
+        const float2 q0 = mul2(x, r2);
+        return fma2(fma2(q0, ns2, x), r2, q0);
     };
 
     if (epi && eok && !*ab.flag) {
@@ -274,45 +262,34 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float x[32];
-                chunk(mt, 0, c, t, x);
+                chunk(mt, c, t, x);
                 uint32_t o[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float2 a = div2(make_float2(x[4 * q], x[4 * q + 1]), rK2, nsK2);
-                    const float2 b = div2(make_float2(x[4 * q + 2], x[4 * q + 3]), rK2, nsK2);
+                    const float2 a = div2(make_float2(x[4 * q], x[4 * q + 1]));
+                    const float2 b = div2(make_float2(x[4 * q + 2], x[4 * q + 3]));
                     o[q] = e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
                 }
                 if (valid) {
-                    // dims 32c .. 32c + 31: two 16-byte chunks of the slot's K-tile row
-                    *reinterpret_cast<uint4*>(krow + ktile_off(slot & 127, 32 * c, D)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(krow + ktile_off(slot & 127, 32 * c + 16, D)) =
-                        make_uint4(o[4], o[5], o[6], o[7]);
-                }
-            }
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float x[32];
-                chunk(mt, 1, c, t, x);
-                uint32_t o[8];
+                    if (kv == 0) {
+                        // dims 32c .. 32c + 31: two 16-byte chunks of the slot's K-tile row
+                        *reinterpret_cast<uint4*>(krow + ktile_off(slot & 127, 32 * c, D)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(krow + ktile_off(slot & 127, 32 * c + 16, D)) =
+                            make_uint4(o[4], o[5], o[6], o[7]);
+                    } else {
+                        // V transposed: dim 32c + e of this slot; the warp's 32
+                        // tokens fill consecutive slots of each dim row
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float2 a = div2(make_float2(x[4 * q], x[4 * q + 1]), rV2, nsV2);
-                    const float2 b = div2(make_float2(x[4 * q + 2], x[4 * q + 3]), rV2, nsV2);
-                    o[q] = e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
-                }
-                if (valid) {
-                    // V transposed: dim 32c + e of this slot; the warp's 32
-                    // tokens fill consecutive slots of each dim row
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        vtile[vtile_off(32 * c + e, slot & 127)] = static_cast<uint8_t>(o[e >> 2] >> (8 * (e & 3)));
+                        for (int e = 0; e < 32; ++e)
+                            vtile[vtile_off(32 * c + e, slot & 127)] =
+                                static_cast<uint8_t>(o[e >> 2] >> (8 * (e & 3)));
+                    }
                 }
             }
             if (valid) {
-                w.sk[static_cast<size_t>(h) * w.Cpad + slot] = sK;
-                w.sv[static_cast<size_t>(h) * w.Cpad + slot] = sV;
-                if (h == 0) w.grp[slot] = w.group;
+                (kv ? w.sv : w.sk)[static_cast<size_t>(h) * w.Cpad + slot] = sc;
+                if (kv == 0 && h == 0) w.grp[slot] = w.group;
             }
         }
     }
@@ -373,7 +350,7 @@ static cudaError_t launch_fused_d(const FusedParams& p, const uint8_t* X, const 
     if (e != cudaSuccess) return e;
     const int nblk = (p.w.n + kFRows - 1) / kFRows;  // <= 8: one portable cluster along the rows
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(nblk, p.w.H);
+    cfg.gridDim = dim3(nblk, p.w.H, 2);  // z: K, V
     cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -62,7 +62,7 @@ struct WriteParams {
 // V = v_mul X Wv^T on the tensor cores, then the write of K2 from the fp32
 // accumulators.  Uses w's ring, scale, group, RoPE and slot fields (w.K and
 // w.V are unused).
-constexpr int kFusedMaxTokens = 2048;  // 8 blocks of 256 rows: one cluster along M
+constexpr int kFusedMaxTokens = 2048;  // 8 blocks of 256 rows: one portable cluster along M
 struct FusedParams {
     WriteParams w;
     float k_mul, v_mul;  // x_scale * wk_scale, x_scale * wv_scale
