@@ -50,8 +50,8 @@ BF16_ROTATE_BYTES = 2.0 * L * H * C * D * 2                # bf16 K read + writt
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attn_kernel launch at
     # the production call, valid while rc_attention.cu has this hash
-    "attention": {"bytes": 87.36e6,
-                  "src_sha256": "e62ad2995516cbadea3bac1e6d7be24aeeb67d49342b1db1b3c0e51d534c965f"},
+    "attention": {"bytes": 87.24e6,
+                  "src_sha256": "2a7c54075c8f90f73de6c85cc14c5a50050f86861b3c90559bb1967596401e6e"},
 }
 
 
@@ -879,6 +879,7 @@ def run_profile_case(kind: str) -> None:
     write     : 3 writes of 757 tokens into 3 layers.
     rotate    : 2 delta rotations of 4 full layers.
     attention_bf16 : the attention case on a bf16 ring.
+    fused     : 3 fused projection writes (757 tokens, hidden 6,144) into 2 layers.
     """
     import numpy as np
     import torch
@@ -886,6 +887,14 @@ def run_profile_case(kind: str) -> None:
     import fp8_ring_kv_cache_gb300 as rc
     import synth_inputs as si
 
+    if kind == "fused":
+        x, xs, wk, wks, wv, wvs = si.proj_operands(23, N_NEW, si.PROD_HIDDEN, H * D, "cuda")
+        cache = rc.RingKVCache(2, H, D, C, max_write=C)
+        for i in range(3):
+            cache.write_fused(i % 2, x, xs, wk, wks, wv, wvs, np.arange(PREFILL, C))
+        cache.sync()
+        print(f"profile case {kind} done, {cache.launch_count} launches")
+        return
     bf16 = kind == "attention_bf16"
     kind = "attention" if bf16 else kind
     nl = {"attention": 2, "write": 3, "rotate": 4}[kind]
@@ -916,7 +925,7 @@ def run_profile_case(kind: str) -> None:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["attention", "write", "rotate", "attention_bf16"], default=None,
+    ap.add_argument("--profile", choices=["attention", "write", "rotate", "attention_bf16", "fused"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
