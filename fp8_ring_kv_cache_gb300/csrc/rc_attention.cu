@@ -518,7 +518,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         const int mt = (warp - kWarpSm0) >> 2;    // M tile of this softmax group
         const int quad = warp & 3;                 // TMEM lane quadrant
         const int r = quad * 32 + lane;            // row within the M tile
-        const int grow = row0 + mt * kMTile + r;   // query row
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + 128u * mt;
         const uint32_t o_tm = tmem + lane_off + 256u + static_cast<uint32_t>(D) * mt;
@@ -799,18 +798,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         if (ok) {
             tc_fence_after();
             const float fin = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            float* orow = p.out + (static_cast<size_t>(grow) * p.H + h) * D;
+            // The warp's 32 rows go out through shared memory (the query
+            // image, free once both M tiles' last Q.K has finished, which
+            // precedes O_DONE on the tensor pipe): each thread parks its row's
+            // 32-column chunk, then each store instruction writes 128-byte
+            // lines of four rows.  A thread storing its own row would touch 32
+            // lines an instruction, a flood that held up the other M tile's
+            // TMEM stores by thousands of cycles.
+            float* stage = reinterpret_cast<float*>(smem + Lay::kQ) + (warp - kWarpSm0) * (32 * 36);
+            const int wrow0 = row0 + mt * kMTile + quad * 32;  // the warp's first query row
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(o_tm + 32 * c, v);
-                if (grow < p.n) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4*>(orow + 32 * c + k) =
-                            make_float4(__uint_as_float(v[k]) * fin, __uint_as_float(v[k + 1]) * fin,
-                                        __uint_as_float(v[k + 2]) * fin, __uint_as_float(v[k + 3]) * fin);
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(stage + lane * 36 + k) =
+                        make_float4(__uint_as_float(v[k]) * fin, __uint_as_float(v[k + 1]) * fin,
+                                    __uint_as_float(v[k + 2]) * fin, __uint_as_float(v[k + 3]) * fin);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + (lane >> 3), q = lane & 7;  // row r of the warp, float4 q
+                    const float4 val = *reinterpret_cast<const float4*>(stage + r * 36 + 4 * q);
+                    if (wrow0 + r < p.n)
+                        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(wrow0 + r) * p.H + h) * D + 32 * c +
+                                                   4 * q) = val;
                 }
+                __syncwarp();
             }
         }
     } else {
