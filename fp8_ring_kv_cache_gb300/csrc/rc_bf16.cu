@@ -425,12 +425,11 @@ __global__ void __launch_bounds__(kBAttnThreads, 1) bf16_attn_kernel(AttnParams 
         }
     } else if (warp >= kBWarpSm0 && warp < kBWarpSmEnd) {
         // ------------------------------------------------------------ softmax
-        // Row r (TMEM lane) of the M tile; scores in log2 units x = S * a with
-        // a = log2(e)/sqrt(D); P = exp2(x - m) in fp16, with the running max m
-        // moved (and O rescaled) only when a tile raises it by more than 8.
+        // Each thread owns one row (TMEM lane) of the M tile; scores in log2
+        // units x = S * a with a = log2(e)/sqrt(D); P = exp2(x - m) in fp16,
+        // with the running max m moved (and O rescaled) only when a tile
+        // raises it by more than 8.
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;
-        const int grow = row0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t o_tm = tmem + lane_off + kBColO;
         const float a = p.sm_log2;
@@ -531,18 +530,32 @@ __global__ void __launch_bounds__(kBAttnThreads, 1) bf16_attn_kernel(AttnParams 
         if (ok) {
             tc_fence_after();
             const float fin = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            float* orow = p.out + (static_cast<size_t>(grow) * p.H + h) * D;
+            // The warp's 32 rows go out through shared memory (the K stages,
+            // free once every MMA has finished, which O_DONE marks): each
+            // thread parks its row's 32-column chunk, then each store
+            // instruction writes 128-byte lines of four rows instead of one
+            // 16-byte piece of 32 rows.
+            float* stage = reinterpret_cast<float*>(smem + Lay::kK) + (warp - kBWarpSm0) * (32 * 36);
+            const int wrow0 = row0 + quad * 32;  // the warp's first query row
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(o_tm + 32 * c, v);
-                if (grow < p.n) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4*>(orow + 32 * c + k) =
-                            make_float4(__uint_as_float(v[k]) * fin, __uint_as_float(v[k + 1]) * fin,
-                                        __uint_as_float(v[k + 2]) * fin, __uint_as_float(v[k + 3]) * fin);
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(stage + lane * 36 + k) =
+                        make_float4(__uint_as_float(v[k]) * fin, __uint_as_float(v[k + 1]) * fin,
+                                    __uint_as_float(v[k + 2]) * fin, __uint_as_float(v[k + 3]) * fin);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + (lane >> 3), q = lane & 7;  // row r of the warp, float4 q
+                    const float4 val = *reinterpret_cast<const float4*>(stage + r * 36 + 4 * q);
+                    if (wrow0 + r < p.n)
+                        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(wrow0 + r) * p.H + h) * D + 32 * c +
+                                                   4 * q) = val;
                 }
+                __syncwarp();
             }
         }
     } else if (warp == kBWarpCheck) {
