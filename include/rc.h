@@ -221,6 +221,8 @@ int rc_cache_set_wait_limit(rc_cache *h, uint64_t ns);
  * 16-byte aligned.  hidden: a multiple of 64.  positions: HOST int64 [n], as
  * for rc_cache_write.  Stream-ordered; the caller keeps X, Wk, Wv alive until
  * the work on `stream` has finished.
+ * A fused write whose kernel gave up a bounded wait (rc_cache_sync then reports
+ * RC_ERR_TIMEOUT) leaves its slots undefined; writing them again repairs them.
  * Errors: RC_ERR_ARG (a pointer NULL or unaligned, layer out of range, n < 1,
  * n > max_write or n > 2048, hidden not a positive multiple of 64, a scale not
  * positive, two tokens on one slot); RC_ERR_UNSUPPORTED with RC_F_BF16_CACHE

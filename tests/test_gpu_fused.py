@@ -148,3 +148,30 @@ def test_fused_errors(rc):
             b.write_fused(0, x, xs, wk, wks, wv, wvs, np.arange(8))
         assert e.value.status == rc.RC_ERR_UNSUPPORTED
     g.sync()
+
+
+def test_fused_wait_runs_out_then_recovers(rc):
+    """Wait limit 0 on the fused write: its first wait whose phase is not
+    complete gives up, every CTA still passes the cluster barriers, drains its
+    copies and MMAs and frees its tensor memory, and rc_cache_sync reports
+    RC_ERR_TIMEOUT.  The write's slots are then undefined; written again with
+    the limit restored they match the oracle (which made the same write twice,
+    so the write serials agree)."""
+    H, D, C, hidden, n = 4, 128, 1200, 512, 700
+    g = rc.RingKVCache(1, H, D, C, max_write=C)
+    o = oracle.OracleCache(1, H, D, C)
+    x, xs, wk, wks, wv, wvs = si.proj_operands(80, n, hidden, H * D, "cuda")
+    pos = np.arange(300, 300 + n)
+    g.set_wait_limit(0)
+    g.write_fused(0, x, xs, wk, wks, wv, wvs, pos)
+    with pytest.raises(rc.RcError) as e:
+        g.sync()
+    assert e.value.status == rc.RC_ERR_TIMEOUT
+    g.sync()  # the record was cleared
+    g.set_wait_limit(2_000_000_000)
+    g.write_fused(0, x, xs, wk, wks, wv, wvs, pos)
+    for _ in range(2):
+        o.write_proj(0, x.cpu(), xs, wk.cpu(), wks, wv.cpu(), wvs, pos)
+    g.sync()
+    check_fused_state(g.export(0), o.export(0), "fused write after a timed-out one")
+    attend_check(g, 0, si.normal_bf16(n, H, D, 81, "cuda"), pos, what="attention after recovery")
