@@ -576,6 +576,7 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
     rp.C = h->C;
     rp.T = h->T;
     rp.Cpad = h->Cpad;
+    rp.wait_ns = h->wait_ns;
     for (int i = 0; i < h->D / 2; ++i) {
         const double ang = static_cast<double>(delta) * h->theta[i];
         rp.cs[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));

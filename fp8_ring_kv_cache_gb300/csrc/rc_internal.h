@@ -78,6 +78,7 @@ struct RotateParams {
     int64_t* slot_pos;     // read-time store [L][Cpad]: moved by delta (nullptr if off)
     int64_t delta;
     int H, C, T, Cpad;
+    uint64_t wait_ns;        // bound of one device wait
     float2 cs[kMaxHalfDim];  // (cos, sin) of delta * theta_i
 };
 

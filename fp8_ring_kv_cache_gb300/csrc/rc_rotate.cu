@@ -214,11 +214,237 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
     }
 }
 
+// ---------------------------------------------------------------- K3, staged
+// The rotation of rings whose share per CTA fits shared memory (T <= 48 tiles
+// at D = 128, 96 at D = 64: the 5,788-slot ring has 46).  Each CTA of the
+// cluster of 8 brings its tiles, with their scales and write groups, into
+// shared memory by one bulk copy per tile, all issued at the start, so HBM sees
+// one read and one write of every code and every read is in flight at once.
+// Both passes then run from shared memory.  A thread takes one 16-byte chunk
+// (16 codes, 8 dimension pairs) of two adjacent slots, so one packed fp32x2
+// instruction rotates a dimension pair of both slots.  The per-group amax
+// table is spread over the cluster: group g's word lives in CTA g % 8, which
+// keeps each CTA's table at Cpad / 8 words and two CTAs on an SM.
+template <int D>
+struct RotStaged {
+    static constexpr int kMaxTiles = (D == 128) ? 6 : 12;  // 96 KB of codes
+    static constexpr uint32_t kTile = kTileSlots * D;
+    static constexpr uint32_t kCodes = 0;
+    static constexpr uint32_t kSk = kMaxTiles * kTile;                    // fp32 [kMaxTiles * 128]
+    static constexpr uint32_t kGrp = kSk + kMaxTiles * kTileSlots * 4;    // int32 [kMaxTiles * 128]
+    static constexpr uint32_t kBar = kGrp + kMaxTiles * kTileSlots * 4;   // mbarrier: the CTA's copies landed
+    static constexpr uint32_t kMisc = kBar + 16;                          // [0] abort flag
+    static constexpr uint32_t kTab = kMisc + 16;                          // uint32 [Cpad / 8] group amax bits
+    static uint32_t bytes(int Cpad) { return kTab + static_cast<uint32_t>(Cpad / kRotCluster) * 4u; }
+};
+
+template <int D>
+__global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThreads, 2)
+    rotate_staged_kernel(RotateParams p, int tpc, int* status) {
+    using Lay = RotStaged<D>;
+    constexpr int CPR = D / 16;              // 16-byte chunks per row
+    constexpr int PPP = kRotThreads / CPR;   // row pairs per pass
+    constexpr int RPP = 2 * PPP;             // rows per pass (64 at D = 128, 128 at D = 64)
+    static_assert(kTileSlots % RPP == 0, "a pass stays inside one tile");
+    extern __shared__ __align__(1024) uint8_t sm[];
+    uint8_t* codes = sm + Lay::kCodes;
+    float* ssk = reinterpret_cast<float*>(sm + Lay::kSk);
+    int32_t* sgrp = reinterpret_cast<int32_t*>(sm + Lay::kGrp);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::kBar);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + Lay::kMisc);
+    uint32_t* tab = reinterpret_cast<uint32_t*>(sm + Lay::kTab);
+
+    const int crank = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int q = tid % CPR;                 // chunk: dims 16 q .. 16 q + 15
+    const int pr = tid / CPR;                // row pair within a pass
+    const int tile0 = min(p.T, crank * tpc);
+    const int ntiles = min(p.T, tile0 + tpc) - tile0;
+    const int row0 = tile0 * kTileSlots;
+    const int nrows = max(0, min(p.C - row0, ntiles * kTileSlots));
+    const size_t lh = static_cast<size_t>(l) * p.H + h;
+    uint8_t* gkc = p.kc + (lh * p.T + tile0) * static_cast<size_t>(Lay::kTile);
+    float* gsk = p.sk + lh * p.Cpad + row0;
+    const int32_t* ggrp = p.grp + static_cast<size_t>(l) * p.Cpad + row0;
+    AbortState ab{reinterpret_cast<volatile uint32_t*>(&misc[0]), status, p.wait_ns};
+
+    // the CTA's tiles are contiguous, and so are their scales and groups:
+    // three bulk copies on one barrier
+    if (tid == 0) {
+        misc[0] = 0u;
+        mbar_init(&bars[0], 1);
+        fence_mbar_init();
+        if (ntiles > 0) {
+            mbar_arrive_expect_tx(&bars[0], ntiles * (Lay::kTile + 2 * kTileSlots * 4));
+            bulk_g2s(codes, gkc, ntiles * Lay::kTile, &bars[0]);
+            bulk_g2s(ssk, gsk, ntiles * kTileSlots * 4, &bars[0]);
+            bulk_g2s(sgrp, ggrp, ntiles * kTileSlots * 4, &bars[0]);
+        }
+    }
+    // (cos, sin) of delta * theta_i through shared memory: indexing the
+    // parameter array per thread would serialise on the constant cache
+    __shared__ float2 s_cs[kMaxHalfDim];
+    if (tid < D / 2) s_cs[tid] = p.cs[tid];
+    for (int i = tid; i < p.Cpad / kRotCluster; i += kRotThreads) tab[i] = 0u;
+    cluster_sync();  // every table is zero before any peer merges into it; the barriers are initialised
+    // the thread's 8 dimension pairs: (c, c), (-s, -s), (s, s)
+    float2 cc[8], ns[8], ss[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 cs = s_cs[q * 8 + j];
+        cc[j] = make_float2(cs.x, cs.x);
+        ns[j] = make_float2(-cs.y, -cs.y);
+        ss[j] = make_float2(cs.y, cs.y);
+    }
+
+    // byte offset of this thread's chunk of row r (r even) and of row r + 1:
+    // the rows have their own swizzle phases
+    auto chunk_off = [&](int r, uint32_t& o0, uint32_t& o1) {
+        const uint32_t base = (r >> 7) * Lay::kTile;
+        o0 = base + ktile_off(r & 127, q * 16, D);
+        o1 = base + ktile_off((r & 127) + 1, q * 16, D);
+    };
+    // rows r and r + 1 of the CTA -> rotated pairs (x of both rows, y of both rows)
+    auto rotate_rows = [&](int r, float2 (&X)[8], float2 (&Y)[8]) {
+        uint32_t o0, o1;
+        chunk_off(r, o0, o1);
+        const uint4 a = *reinterpret_cast<const uint4*>(codes + o0);
+        const uint4 b = *reinterpret_cast<const uint4*>(codes + o1);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float2 va = e4m3x2_to_float2(static_cast<uint16_t>(wa[j >> 1] >> (16 * (j & 1))));
+            const float2 vb = e4m3x2_to_float2(static_cast<uint16_t>(wb[j >> 1] >> (16 * (j & 1))));
+            const float2 x = make_float2(va.x, vb.x), y = make_float2(va.y, vb.y);
+            // the rounding order of rotate_pair: the y products first, then fused into x (c, s)
+            X[j] = fma2(x, cc[j], mul2(y, ns[j]));
+            Y[j] = fma2(x, ss[j], mul2(y, cc[j]));
+        }
+    };
+    static_assert(D == 128 || D == 64, "head_dim 64 or 128");
+
+    bool ok = true;
+    // ---- pass 1: rotated amax per write group, a running max flushed per run of rows
+    float acc = 0.f, scur = 0.f;
+    int gcur = -1;
+    auto flush = [&]() {
+        if (gcur >= 0) dsmem_max_u32(map_shared(&tab[gcur >> 3], gcur & 7), __float_as_uint(acc * scur));
+    };
+    if (ntiles > 0) ok = mbar_wait(&bars[0], 0, ab, kDevTimeoutLoader);
+    for (int i = 0; i < ntiles && ok; ++i) {
+#pragma unroll 1
+        for (int rb = i * kTileSlots; rb < (i + 1) * kTileSlots; rb += RPP) {
+            const int r = rb + 2 * pr;
+            const int g0 = (r < nrows) ? sgrp[r] : -1;
+            const int g1 = (r + 1 < nrows) ? sgrp[r + 1] : -1;
+            if (g0 < 0 && g1 < 0) continue;
+            float2 X[8], Y[8];
+            rotate_rows(r, X, Y);
+            float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                m0 = max3(m0, fabsf(X[j].x), fabsf(Y[j].x));
+                m1 = max3(m1, fabsf(X[j].y), fabsf(Y[j].y));
+                m2 = max3(m2, fabsf(X[j + 1].x), fabsf(Y[j + 1].x));
+                m3 = max3(m3, fabsf(X[j + 1].y), fabsf(Y[j + 1].y));
+            }
+            const float mr[2] = {fmaxf(m0, m2), fmaxf(m1, m3)};
+            const int gr[2] = {g0, g1};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (gr[k] < 0) continue;
+                if (gr[k] != gcur) {
+                    flush();
+                    gcur = gr[k];
+                    scur = ssk[r + k];
+                    acc = 0.f;
+                }
+                acc = fmaxf(acc, mr[k]);
+            }
+        }
+    }
+    if (ok) flush();
+    __syncwarp();
+    cluster_sync();  // every merge has landed
+    // ---- each row's new scale s = fl32(amax / 448) (stored) and its factor
+    // fl32(s_old / s) (kept in ssk for pass 2): the only reads of the peers'
+    // tables, after which this CTA arrives at the exit barrier
+    if (ok) {
+        for (int r = tid; r < nrows; r += kRotThreads) {
+            const int g = sgrp[r];
+            if (g < 0) continue;
+            const float amax = __uint_as_float(dsmem_ld_u32(map_shared(&tab[g >> 3], g & 7)));
+            const float snew = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
+            gsk[r] = snew;
+            ssk[r] = __fdiv_rn(ssk[r], snew);
+        }
+    }
+    __syncwarp();
+    cluster_arrive_release();
+    __syncthreads();
+    // ---- pass 2: requantise with the group's new scale, in place
+    for (int i = 0; i < ntiles && ok; ++i) {
+#pragma unroll 1
+        for (int rb = i * kTileSlots; rb < (i + 1) * kTileSlots; rb += RPP) {
+            const int r = rb + 2 * pr;
+            const int g0 = (r < nrows) ? sgrp[r] : -1;
+            const int g1 = (r + 1 < nrows) ? sgrp[r + 1] : -1;
+            if (g0 < 0 && g1 < 0) continue;
+            const float u0 = (g0 >= 0) ? ssk[r] : 0.f, u1 = (g1 >= 0) ? ssk[r + 1] : 0.f;
+            float2 X[8], Y[8];
+            rotate_rows(r, X, Y);
+            const float2 u = make_float2(u0, u1);
+            uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 x = mul2(X[j], u), y = mul2(Y[j], u);
+                wa[j >> 1] |= e4m3x2(x.x, y.x) << (16 * (j & 1));
+                wb[j >> 1] |= e4m3x2(x.y, y.y) << (16 * (j & 1));
+            }
+            uint32_t o0, o1;
+            chunk_off(r, o0, o1);
+            if (g0 >= 0) *reinterpret_cast<uint4*>(gkc + o0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            if (g1 >= 0) *reinterpret_cast<uint4*>(gkc + o1) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        }
+    }
+    // the read-time ablation's copy of each slot's position moves with it
+    if (ok && p.slot_pos != nullptr && h == 0) {
+        int64_t* spos = p.slot_pos + static_cast<size_t>(l) * p.Cpad + row0;
+        for (int r = tid; r < nrows; r += kRotThreads)
+            if (sgrp[r] >= 0) spos[r] += p.delta;
+    }
+    if (!ok && tid == 0 && ntiles > 0) {
+        // leave no copy in flight into this CTA's shared memory (bounded)
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars[0], 0) && global_timer_ns() - t0 < 100000000ull) {
+        }
+    }
+    __syncwarp();
+    cluster_wait();  // every peer has read this CTA's table
+}
+
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status) {
     const int tpc = (p.T + kRotCluster - 1) / kRotCluster;
-    const size_t smem = static_cast<size_t>(p.Cpad) * 4;
     dim3 grid(kRotCluster, p.H, layers);
     cudaError_t e;
+    if (tpc <= ((D == 128) ? RotStaged<128>::kMaxTiles : RotStaged<64>::kMaxTiles)) {
+        static std::atomic<uint64_t> done128{0}, done64{0};
+        if (D == 128) {
+            const uint32_t smem = RotStaged<128>::bytes(p.Cpad);
+            e = smem_limit_once(rotate_staged_kernel<128>, RotStaged<128>::bytes(kRotCluster * RotStaged<128>::kMaxTiles * kTileSlots),
+                                done128);
+            if (e != cudaSuccess) return e;
+            rotate_staged_kernel<128><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
+        } else {
+            const uint32_t smem = RotStaged<64>::bytes(p.Cpad);
+            e = smem_limit_once(rotate_staged_kernel<64>, RotStaged<64>::bytes(kRotCluster * RotStaged<64>::kMaxTiles * kTileSlots),
+                                done64);
+            if (e != cudaSuccess) return e;
+            rotate_staged_kernel<64><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
+        }
+        return cudaGetLastError();
+    }
+    const size_t smem = static_cast<size_t>(p.Cpad) * 4;
     if (D == 128) {
         e = cudaFuncSetAttribute(rotate_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
