@@ -257,6 +257,36 @@ def test_delta_one_step_multilayer(rc):
     assert g.delta_total == -137 - 99999 + 5
 
 
+@pytest.mark.parametrize("D,C", [(128, 6144), (128, 6200), (64, 10240), (64, 10300)])
+def test_delta_both_rotation_kernels(rc, D, C):
+    # A CTA of the rotation's cluster of 8 stages its share of a head's tiles
+    # in shared memory while that share is at most 6 tiles (D = 128) or 10
+    # (D = 64): rings of up to 6,144 / 10,240 slots.  Larger rings take the
+    # two-pass kernel.  Both sides of each limit, with a wrapping write and
+    # groups of different scales, checked one step at a time.
+    H = 2
+    g = rc.RingKVCache(1, H, D, C, max_write=C)
+    o = oracle.OracleCache(1, H, D, C)
+    p = 0
+    for i, n in enumerate([C - 700, 900, 450]):
+        k = si.normal_bf16(n, H, D, 3000 + i, "cuda", mult=torch.full((H, 1), 0.5 + i))
+        v = si.normal_bf16(n, H, D, 3100 + i, "cuda")
+        g.write(0, k, v, np.arange(p, p + n))
+        o.write(0, k.cpu(), v.cpu(), np.arange(p, p + n))
+        p += n
+    g.sync()
+    st = g.export(0)
+    check_state(st, o.export(0), f"C={C} before")
+    o.import_layer(0, st, o.last_positions(0), o.delta_total, 4)
+    for delta in (-4321, 77):
+        g.delta_rotate(delta)
+        o.delta_rotate(delta)
+        g.sync()
+        st = g.export(0)
+        check_state(st, o.export(0), f"C={C} after delta {delta}")
+        o.import_layer(0, st, o.last_positions(0), o.delta_total, 4)
+
+
 def test_memory_stable_across_write_sizes(rc):
     C = si.PROD_SLOTS
     g = rc.RingKVCache(1, 8, 128, C)
