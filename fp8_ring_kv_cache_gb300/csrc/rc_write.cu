@@ -46,7 +46,6 @@ constexpr int kWriteCluster = 8;
 constexpr int kWriteWarps = 8;
 constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kWriteTB = 96;  // tokens staged in shared memory per batch
-constexpr int kWritePer = kWriteTB / kWriteWarps;  // tokens a warp takes per batch
 
 template <int D>
 struct WriteSmem {
@@ -62,7 +61,15 @@ template <int D>
 __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteThreads, 3)
     write_kernel(WriteParams p) {
     using S = WriteSmem<D>;
-    constexpr int EPL = D / 32;       // elements per lane (4 or 2)
+    // A token is taken by CPT lanes, each with 16 of its dims: [8c, 8c + 8) and
+    // [D/2 + 8c, D/2 + 8c + 8) for lane chunk c, so the 16-byte shared reads of
+    // a token's row are contiguous across its lanes.  A warp takes TPS tokens
+    // a step, and the per-token work (slot, tile address, scale stores) is
+    // shared by TPS tokens of one instruction.
+    constexpr int CPT = D / 16;                         // lanes per token
+    constexpr int TPS = 32 / CPT;                       // tokens a warp takes per step
+    constexpr int TPB = kWriteWarps * TPS;              // tokens the CTA takes per step
+    constexpr int kSteps = (kWriteTB + TPB - 1) / TPB;  // steps per staged batch
     constexpr int HALF = D / 2;
     constexpr uint32_t ROWB = D * 2;  // bytes of one bf16 head row
     extern __shared__ __align__(128) uint8_t smem[];
@@ -76,11 +83,11 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     const int h = blockIdx.y;
     const int crank = blockIdx.x;     // the cluster spans blockIdx.x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ts = lane / CPT, c = lane % CPT;  // the lane's token within the warp's step, its chunk
     const int tpc = (p.n + kWriteCluster - 1) / kWriteCluster;
     const int t0 = min(p.n, crank * tpc);
     const int t1 = min(p.n, t0 + tpc);
     const int nbatch = (t1 - t0 + kWriteTB - 1) / kWriteTB;
-    const int dim0 = lane * EPL;
     // every CTA of the cluster is running once this barrier phase completes
     cluster_arrive_relaxed();
 
@@ -100,41 +107,50 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         const int total = cnt * 2 * kUnits;
         for (int u = threadIdx.x; u < total; u += kWriteThreads) {
             const int tl = u / (2 * kUnits), r = u - tl * (2 * kUnits);
-            const int which = r / kUnits, c = r - which * kUnits;
-            const __nv_bfloat16* src = (which ? p.V : p.K) + (static_cast<size_t>(tb + tl) * p.H + h) * D + c * 8;
-            __nv_bfloat16* dst = (which ? vbuf : kbuf) + tl * D + c * 8;
+            const int which = r / kUnits, cc = r - which * kUnits;
+            const __nv_bfloat16* src = (which ? p.V : p.K) + (static_cast<size_t>(tb + tl) * p.H + h) * D + cc * 8;
+            __nv_bfloat16* dst = (which ? vbuf : kbuf) + tl * D + cc * 8;
             cp_async16(dst, src);
         }
         cp_async_wait_all();
         __syncthreads();
     };
-    // cos/sin pairs of this lane's dims for the warp's tokens of a batch, all
-    // loads in flight at once (one L2 round trip instead of one per token)
-    auto fetch_rope = [&](int tb, int cnt, float2 (&cs)[kWritePer][EPL / 2]) {
+    // batch-local token of this lane in step st (the last step may run past cnt)
+    auto tok = [&](int st) { return st * TPB + warp * TPS + ts; };
+    // (cos, sin) of the lane's 8 dimension pairs for every step of a batch, all
+    // loads in flight at once: pairs 4c..4c+3 and D/4 + 4c..D/4 + 4c + 3, two
+    // pairs a float4
+    auto fetch_rope = [&](int tb, int cnt, float4 (&cs)[kSteps][4]) {
 #pragma unroll
-        for (int i = 0; i < kWritePer; ++i) {
-            const int tl = warp + kWriteWarps * i;
-            const float2* rr = p.rope + static_cast<size_t>(tb + min(tl, cnt - 1)) * HALF + dim0 / 2;
-#pragma unroll
-            for (int j = 0; j < EPL / 2; ++j) cs[i][j] = __ldg(rr + j);
+        for (int st = 0; st < kSteps; ++st) {
+            const float4* rr =
+                reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(tb + min(tok(st), cnt - 1)) * HALF);
+            cs[st][0] = __ldg(rr + 2 * c);
+            cs[st][1] = __ldg(rr + 2 * c + 1);
+            cs[st][2] = __ldg(rr + D / 8 + 2 * c);
+            cs[st][3] = __ldg(rr + D / 8 + 2 * c + 1);
         }
     };
-    // token tl of the staged batch: K rotated at its position (EPL values of this lane) and V
-    auto row = [&](int tl, const float2 (&cs)[EPL / 2], float (&k)[EPL], float (&v)[EPL]) {
-        __nv_bfloat16 kb[EPL], vb[EPL];
-        if constexpr (EPL == 4) {
-            *reinterpret_cast<uint2*>(kb) = *reinterpret_cast<const uint2*>(kbuf + tl * D + dim0);
-            *reinterpret_cast<uint2*>(vb) = *reinterpret_cast<const uint2*>(vbuf + tl * D + dim0);
-        } else {
-            *reinterpret_cast<uint32_t*>(kb) = *reinterpret_cast<const uint32_t*>(kbuf + tl * D + dim0);
-            *reinterpret_cast<uint32_t*>(vb) = *reinterpret_cast<const uint32_t*>(vbuf + tl * D + dim0);
+    // the lane's 16 dims of token tl: K rotated at its position, and V; word i
+    // of a row piece holds dims (2i, 2i + 1), pair i of the lane
+    auto row = [&](int tl, const float4 (&cs)[4], float (&k)[16], float (&v)[16]) {
+        const uint8_t* kr = reinterpret_cast<const uint8_t*>(kbuf + tl * D);
+        const uint8_t* vr = reinterpret_cast<const uint8_t*>(vbuf + tl * D);
+        const uint4 k0 = *reinterpret_cast<const uint4*>(kr + 16 * c);
+        const uint4 k1 = *reinterpret_cast<const uint4*>(kr + D + 16 * c);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(vr + 16 * c);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(vr + D + 16 * c);
+        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float cc = (i & 1) ? cs[i >> 1].z : cs[i >> 1].x;
+            const float ss = (i & 1) ? cs[i >> 1].w : cs[i >> 1].y;
+            rotate_pair(__uint_as_float(kw[i] << 16), __uint_as_float(kw[i] & 0xFFFF0000u), cc, ss, k[2 * i],
+                        k[2 * i + 1]);
+            v[2 * i] = __uint_as_float(vw[i] << 16);
+            v[2 * i + 1] = __uint_as_float(vw[i] & 0xFFFF0000u);
         }
-#pragma unroll
-        for (int j = 0; j < EPL / 2; ++j)
-            rotate_pair(__bfloat162float(kb[2 * j]), __bfloat162float(kb[2 * j + 1]), cs[j].x, cs[j].y, k[2 * j],
-                        k[2 * j + 1]);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) v[e] = __bfloat162float(vb[e]);
     };
 
     // ---- phase 1: per-head amax of rotated K and of V over this CTA's tokens
@@ -142,34 +158,34 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     for (int b = 0; b < nbatch; ++b) {
         const int tb = t0 + b * kWriteTB;
         const int cnt = min(kWriteTB, t1 - tb);
-        float2 cs[kWritePer][EPL / 2];
+        float4 cs[kSteps][4];
         fetch_rope(tb, cnt, cs);
         stage_batch(tb, cnt);
-        {
 #pragma unroll
-            for (int i = 0; i < kWritePer; ++i) {
-                // past the batch's end a warp repeats its last token, which the max
-                // already holds: no branch, so the tokens' work can overlap
-                const int tl = warp + kWriteWarps * i;
-                if (tl >= cnt) break;
-                float k[EPL], v[EPL];
-                row(tl, cs[i], k, v);
+        for (int st = 0; st < kSteps; ++st) {
+            if (st * TPB + warp * TPS >= cnt) break;  // warp-uniform
+            // a lane past the batch's end repeats the last token, which the max
+            // already holds: no branch
+            const int tl = min(tok(st), cnt - 1);
+            float k[16], v[16];
+            row(tl, cs[st], k, v);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    amk = fmaxf(amk, fabsf(k[e]));
-                    amv = fmaxf(amv, fabsf(v[e]));
-                }
-                if (p.kraw != nullptr && warp + kWriteWarps * i < cnt) {
-                    // read-time ablation store: the unrotated bf16 row and the slot's position
-                    const int slot = slot_of(tb + tl);
-                    const size_t dst = (static_cast<size_t>(h) * p.Cpad + slot) * D + dim0;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) {
-                        p.kraw[dst + e] = kbuf[tl * D + dim0 + e];
-                        p.vraw[dst + e] = vbuf[tl * D + dim0 + e];
-                    }
-                    if (h == 0 && lane == 0) p.slot_pos[slot] = p.pos ? p.pos[tb + tl] : p.p0 + tb + tl;
-                }
+            for (int e = 0; e < 16; e += 2) {
+                amk = max3(amk, fabsf(k[e]), fabsf(k[e + 1]));
+                amv = max3(amv, fabsf(v[e]), fabsf(v[e + 1]));
+            }
+            if (p.kraw != nullptr && tok(st) < cnt) {
+                // read-time ablation store: the unrotated bf16 row and the slot's position
+                const int slot = slot_of(tb + tl);
+                uint8_t* kd = reinterpret_cast<uint8_t*>(p.kraw + (static_cast<size_t>(h) * p.Cpad + slot) * D);
+                uint8_t* vd = reinterpret_cast<uint8_t*>(p.vraw + (static_cast<size_t>(h) * p.Cpad + slot) * D);
+                const uint8_t* kr = reinterpret_cast<const uint8_t*>(kbuf + tl * D);
+                const uint8_t* vr = reinterpret_cast<const uint8_t*>(vbuf + tl * D);
+                *reinterpret_cast<uint4*>(kd + 16 * c) = *reinterpret_cast<const uint4*>(kr + 16 * c);
+                *reinterpret_cast<uint4*>(kd + D + 16 * c) = *reinterpret_cast<const uint4*>(kr + D + 16 * c);
+                *reinterpret_cast<uint4*>(vd + 16 * c) = *reinterpret_cast<const uint4*>(vr + 16 * c);
+                *reinterpret_cast<uint4*>(vd + D + 16 * c) = *reinterpret_cast<const uint4*>(vr + D + 16 * c);
+                if (h == 0 && c == 0) p.slot_pos[slot] = p.pos ? p.pos[tb + tl] : p.p0 + tb + tl;
             }
         }
         __syncthreads();  // the next batch overwrites the staging buffers
@@ -187,7 +203,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     // ---- across the cluster: each CTA pushes its two maxima into every CTA's
     // table, one barrier makes them visible, and every thread reads its own table
     // phase 2's first angles are on their way while the cluster agrees on the scales
-    float2 cs[kWritePer][EPL / 2];
+    float4 cs[kSteps][4];
     if (nbatch > 0) fetch_rope(t0, min(kWriteTB, t1 - t0), cs);
     cluster_wait();  // (the arrival at kernel start) every CTA is running
     if (threadIdx.x < 2 * kWriteCluster) {
@@ -222,41 +238,38 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         if (b > 0) fetch_rope(tb, cnt, cs);
         if (nbatch > 1) stage_batch(tb, cnt);
 #pragma unroll
-        for (int i = 0; i < kWritePer; ++i) {
-            // past the batch's end a warp repeats its last token's stores (same
-            // values to the same places) into staging rows nobody reads
-            const int tw = warp + kWriteWarps * i, tl = tw;
-            if (tl >= cnt) break;
-            float k[EPL], v[EPL];
-            row(tl, cs[i], k, v);
+        for (int st = 0; st < kSteps; ++st) {
+            if (st * TPB + warp * TPS >= cnt) break;  // warp-uniform
+            const int tw = tok(st);
+            const bool live = tw < cnt;
+            const int tl = min(tw, cnt - 1);
+            float k[16], v[16];
+            row(tl, cs[st], k, v);
             const int slot = slot_of(tb + tl);
-            if (lane == 0) sslot[tw] = slot;
-            uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
-            float qk[EPL], qv[EPL];
+            uint32_t kq[8], vq[8];  // codes of pairs i (16 bits each)
 #pragma unroll
-            for (int e = 0; e < EPL; e += 2) {
-                const float2 a = div2(make_float2(k[e], k[e + 1]), rK2, nsK2);
-                const float2 b = div2(make_float2(v[e], v[e + 1]), rV2, nsV2);
-                qk[e] = a.x;
-                qk[e + 1] = a.y;
-                qv[e] = b.x;
-                qv[e + 1] = b.y;
+            for (int i = 0; i < 8; ++i) {
+                const float2 a = div2(make_float2(k[2 * i], k[2 * i + 1]), rK2, nsK2);
+                const float2 bq = div2(make_float2(v[2 * i], v[2 * i + 1]), rV2, nsV2);
+                kq[i] = e4m3x2(a.x, a.y);
+                vq[i] = e4m3x2(bq.x, bq.y);
             }
-            if constexpr (EPL == 4) {
-                *reinterpret_cast<uint32_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
-                    e4m3x2(qk[0], qk[1]) | (e4m3x2(qk[2], qk[3]) << 16);
-                *reinterpret_cast<uint32_t*>(vstage + tw * S::kVRow + dim0) =
-                    e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
-            } else {
-                *reinterpret_cast<uint16_t*>(ktile + ktile_off(slot & 127, dim0, D)) =
-                    static_cast<uint16_t>(e4m3x2(qk[0], qk[1]));
-                *reinterpret_cast<uint16_t*>(vstage + tw * S::kVRow + dim0) =
-                    static_cast<uint16_t>(e4m3x2(qv[0], qv[1]));
-            }
-            if (lane == 0) {
-                p.sk[static_cast<size_t>(h) * p.Cpad + slot] = sK;
-                p.sv[static_cast<size_t>(h) * p.Cpad + slot] = sV;
-                if (h == 0) p.grp[slot] = p.group;
+            if (live) {
+                uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
+                *reinterpret_cast<uint2*>(ktile + ktile_off(slot & 127, 8 * c, D)) =
+                    make_uint2(kq[0] | (kq[1] << 16), kq[2] | (kq[3] << 16));
+                *reinterpret_cast<uint2*>(ktile + ktile_off(slot & 127, HALF + 8 * c, D)) =
+                    make_uint2(kq[4] | (kq[5] << 16), kq[6] | (kq[7] << 16));
+                *reinterpret_cast<uint2*>(vstage + tw * S::kVRow + 8 * c) =
+                    make_uint2(vq[0] | (vq[1] << 16), vq[2] | (vq[3] << 16));
+                *reinterpret_cast<uint2*>(vstage + tw * S::kVRow + HALF + 8 * c) =
+                    make_uint2(vq[4] | (vq[5] << 16), vq[6] | (vq[7] << 16));
+                if (c == 0) {
+                    sslot[tw] = slot;
+                    p.sk[static_cast<size_t>(h) * p.Cpad + slot] = sK;
+                    p.sv[static_cast<size_t>(h) * p.Cpad + slot] = sV;
+                    if (h == 0) p.grp[slot] = p.group;
+                }
             }
         }
         __syncthreads();
