@@ -390,11 +390,6 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-// Arrival that publishes this thread's earlier memory operations to the
-// cluster (pairs with the acquire of cluster_wait).
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }

@@ -379,8 +379,12 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
             ssk[r] = __fdiv_rn(ssk[r], snew);
         }
     }
+    // the arrival only says "done reading the peers' tables": the reads have
+    // completed (their values are used above), and nothing this CTA wrote needs
+    // ordering for the peers, so it is relaxed (a release would wait for the
+    // scale stores)
     __syncwarp();
-    cluster_arrive_release();
+    cluster_arrive_relaxed();
     __syncthreads();
     // ---- pass 2: requantise with the group's new scale, in place
     for (int i = 0; i < ntiles && ok; ++i) {
