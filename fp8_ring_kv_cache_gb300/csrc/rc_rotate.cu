@@ -218,13 +218,15 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
 // The rotation of rings whose share per CTA fits shared memory (T <= 48 tiles
 // at D = 128, 96 at D = 64: the 5,788-slot ring has 46).  Each CTA of the
 // cluster of 8 brings its tiles, with their scales and write groups, into
-// shared memory by one bulk copy per tile, all issued at the start, so HBM sees
-// one read and one write of every code and every read is in flight at once.
+// shared memory by three bulk copies issued at the start, so HBM sees one read
+// and one write of every code and every read is in flight at once.
 // Both passes then run from shared memory.  A thread takes one 16-byte chunk
 // (16 codes, 8 dimension pairs) of two adjacent slots, so one packed fp32x2
 // instruction rotates a dimension pair of both slots.  The per-group amax
 // table is spread over the cluster: group g's word lives in CTA g % 8, which
 // keeps each CTA's table at Cpad / 8 words and two CTAs on an SM.
+constexpr uint64_t kStaggerNs = 4000;  // start spacing of the staged rotation's first wave
+
 template <int D>
 struct RotStaged {
     static constexpr int kMaxTiles = (D == 128) ? 6 : 12;  // 96 KB of codes
@@ -240,7 +242,7 @@ struct RotStaged {
 
 template <int D>
 __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThreads, 2)
-    rotate_staged_kernel(RotateParams p, int tpc, int* status) {
+    rotate_staged_kernel(RotateParams p, int tpc, int wave, int* status) {
     using Lay = RotStaged<D>;
     constexpr int CPR = D / 16;              // 16-byte chunks per row
     constexpr int PPP = kRotThreads / CPR;   // row pairs per pass
@@ -274,6 +276,17 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
         misc[0] = 0u;
         mbar_init(&bars[0], 1);
         fence_mbar_init();
+        // The first wave's clusters (the `wave` clusters resident at once)
+        // would otherwise run their phases in lockstep for the whole launch:
+        // every CTA loading at once, then every CTA requantising.  Holding
+        // their copies back by 0, 4, 8 or 12 us lets the loads of some
+        // clusters overlap the stores of others from then on.
+        const int cid = blockIdx.y + blockIdx.z * gridDim.y;
+        if (cid < wave) {
+            const uint64_t hold = static_cast<uint64_t>(cid & 3) * kStaggerNs;
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < hold) __nanosleep(256);
+        }
         if (ntiles > 0) {
             mbar_arrive_expect_tx(&bars[0], ntiles * (Lay::kTile + 2 * kTileSlots * 4));
             bulk_g2s(codes, gkc, ntiles * Lay::kTile, &bars[0]);
@@ -427,24 +440,55 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
     cluster_wait();  // every peer has read this CTA's table
 }
 
+// Clusters of the staged kernel resident at once on this device (its largest
+// shared-memory size), kept per device; 0 where the query fails.
+template <int D>
+static int staged_wave(uint32_t smem) {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n != 0) return n > 0 ? n : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRotCluster, 64, 1);
+    cfg.blockDim = dim3(kRotThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaOccupancyMaxActiveClusters(&n, rotate_staged_kernel<D>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = -1;
+    }
+    cached[dev].store(n, std::memory_order_release);
+    return n > 0 ? n : 0;
+}
+
 cudaError_t launch_rotate(const RotateParams& p, int D, int layers, cudaStream_t s, int* status) {
     const int tpc = (p.T + kRotCluster - 1) / kRotCluster;
     dim3 grid(kRotCluster, p.H, layers);
     cudaError_t e;
     if (tpc <= ((D == 128) ? RotStaged<128>::kMaxTiles : RotStaged<64>::kMaxTiles)) {
         static std::atomic<uint64_t> done128{0}, done64{0};
+        // the stagger pays off over many waves only: a grid of fewer than
+        // four waves starts at once
+        const long clusters = static_cast<long>(p.H) * layers;
         if (D == 128) {
             const uint32_t smem = RotStaged<128>::bytes(p.Cpad);
-            e = smem_limit_once(rotate_staged_kernel<128>, RotStaged<128>::bytes(kRotCluster * RotStaged<128>::kMaxTiles * kTileSlots),
-                                done128);
+            const uint32_t most = RotStaged<128>::bytes(kRotCluster * RotStaged<128>::kMaxTiles * kTileSlots);
+            e = smem_limit_once(rotate_staged_kernel<128>, most, done128);
             if (e != cudaSuccess) return e;
-            rotate_staged_kernel<128><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
+            int wave = staged_wave<128>(most);
+            if (clusters < 4L * wave) wave = 0;
+            rotate_staged_kernel<128><<<grid, kRotThreads, smem, s>>>(p, tpc, wave, status);
         } else {
             const uint32_t smem = RotStaged<64>::bytes(p.Cpad);
-            e = smem_limit_once(rotate_staged_kernel<64>, RotStaged<64>::bytes(kRotCluster * RotStaged<64>::kMaxTiles * kTileSlots),
-                                done64);
+            const uint32_t most = RotStaged<64>::bytes(kRotCluster * RotStaged<64>::kMaxTiles * kTileSlots);
+            e = smem_limit_once(rotate_staged_kernel<64>, most, done64);
             if (e != cudaSuccess) return e;
-            rotate_staged_kernel<64><<<grid, kRotThreads, smem, s>>>(p, tpc, status);
+            int wave = staged_wave<64>(most);
+            if (clusters < 4L * wave) wave = 0;
+            rotate_staged_kernel<64><<<grid, kRotThreads, smem, s>>>(p, tpc, wave, status);
         }
         return cudaGetLastError();
     }
