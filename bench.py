@@ -135,6 +135,46 @@ def job_throughput(world: int, steps: int, elapsed_ms: float) -> float:
     return world * CALLS_PER_CHUNK * steps / (elapsed_ms / 1e3)
 
 
+def capture_graph(fn, side):
+    """The launches of fn() captured into a CUDA graph on stream `side` (not
+    launched).  The library's host-side bookkeeping (slots, write groups) runs
+    as in a direct call, so the graph holds exactly the kernels a direct call
+    would launch, with the same arguments; it is launched once, in order."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        g.capture_begin(capture_error_mode="thread_local")
+        try:
+            fn()
+        finally:
+            g.capture_end()
+    return g
+
+
+def graphed_ms(fn, n: int, stream) -> float:
+    """Device time of n calls of fn, each captured into its own CUDA graph and
+    launched once on `stream`: the host captures call i + 1 while the GPU runs
+    call i, and the first graph is captured before the clock starts.  Events
+    on `stream` bracket the n launches."""
+    import torch
+
+    side = torch.cuda.Stream()
+    done = []
+    g = capture_graph(fn, side)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(n):
+        with torch.cuda.stream(stream):
+            g.replay()
+        done.append(g)
+        if i + 1 < n:
+            g = capture_graph(fn, side)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
@@ -193,43 +233,38 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     for _ in range(args.warmup):
         step()
+    graphed_ms(step, 1, stream)  # the capture path warmed up too
     cache.sync()
 
-    # ---- timed region: K steps, per-kernel events on the launching stream
-    nw = args.steps * CALLS_PER_CHUNK
-    rec = {"w": [(ev(), ev()) for _ in range(nw)], "a": [(ev(), ev()) for _ in range(nw)],
-           "r": [(ev(), ev()) for _ in range(args.steps)], "i": 0, "j": 0}
+    # ---- timed region: K steps, each a CUDA graph launched once
     launches0 = cache.launch_count
     clocks = ClockSampler(local_rank)
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t0, t1 = ev(), ev()
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(rec)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms = graphed_ms(step, args.steps, stream)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     cache.sync()
     launches = cache.launch_count - launches0
-    elapsed_ms = t0.elapsed_time(t1)
+
+    # ---- per-kernel times: K more steps launched directly, events around every call
+    nw = args.steps * CALLS_PER_CHUNK
+    rec = {"w": [(ev(), ev()) for _ in range(nw)], "a": [(ev(), ev()) for _ in range(nw)],
+           "r": [(ev(), ev()) for _ in range(args.steps)], "i": 0, "j": 0}
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        step(rec)
+    torch.cuda.synchronize()
+    cache.sync()
     w_times = [a.elapsed_time(b) * 1e3 for a, b in rec["w"]]
     a_times = [a.elapsed_time(b) * 1e3 for a, b in rec["a"]]
     r_times = [a.elapsed_time(b) * 1e3 for a, b in rec["r"]]
 
-    # ---- chunk without a reset (ms per 240-call chunk), same inputs
-    torch.cuda.synchronize()
-    c0, c1 = ev(), ev()
-    c0.record(stream)
-    for _ in range(args.steps):
-        chunk()
-    c1.record(stream)
-    torch.cuda.synchronize()
-    chunk_ms = c0.elapsed_time(c1) / args.steps
+    # ---- chunk without a reset (ms per 240-call chunk), same inputs, graphs as above
+    chunk_ms = graphed_ms(chunk, args.steps, stream) / args.steps
     cache.sync()
     del cache
 
@@ -285,6 +320,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "calls_per_step": CALLS_PER_CHUNK, "outliers": "1% of (head, channel) pairs x20 on K and V",
             "l2": "no flush: 4.3 GB of rings and 6.7 GB of chunk inputs per step exceed the 129 MB L2",
             "parallelism": f"replicas x{world} (one session per GPU)",
+            "launch": "each step captured into a CUDA graph (the host captures step k + 1 while the GPU runs "
+                      "step k) and launched once; per-kernel times from as many steps launched directly",
         },
         "ms_per_chunk": round(chunk_ms, 4),
         "roofline": {
@@ -330,9 +367,11 @@ def run_sustained(args) -> dict:
     U[0.5, 4] for Q, K and V alike (the 240 distinct inputs of a chunk are
     generated once and reused).  Each chunk writes 757 new positions (4 passes
     rewrite them) and the window restarts every 300 chunks: one delta rotation
-    of every layer by -(oldest stored position).  Per-chunk times come from
-    events on the launching stream; the steady state leaves out the first
-    three chunks (the ring fills during the first)."""
+    of every layer by -(oldest stored position).  Each chunk is captured into a
+    CUDA graph while the GPU runs the previous one and launched once; per-chunk
+    times come from events around the launches on the launching stream; the
+    steady state leaves out the first three chunks (the ring fills during the
+    first)."""
     import numpy as np
     import torch
 
@@ -366,15 +405,24 @@ def run_sustained(args) -> dict:
     clocks = ClockSampler(0, period_ms=500)
     clocks.start()
     launches0 = cache.launch_count
-    t0 = time.perf_counter()
-    for c in range(nch):
-        pos = np.arange(newest + 1, newest + 1 + N_NEW)
-        ev[c][0].record(stream)
+    side = torch.cuda.Stream()
+
+    def chunk(pos):
         for pas in range(PASSES):
             for layer in range(L):
                 cache.write(layer, K[pas, layer], V[pas, layer], pos)
                 cache.attend(layer, Q[pas, layer], out)
+
+    # the host's calls keep the device's order: chunk c's graph is launched
+    # (and the reset after it made) before chunk c + 1 is captured
+    t0 = time.perf_counter()
+    g = capture_graph(lambda: chunk(np.arange(newest + 1, newest + 1 + N_NEW)), side)
+    recent = []
+    for c in range(nch):
+        ev[c][0].record(stream)
+        g.replay()
         ev[c][1].record(stream)
+        recent = (recent + [g])[-4:]     # a graph freed in flight is released when it completes
         newest += N_NEW
         if (c + 1) % every == 0:
             oldest = newest - C + 1          # the ring is full after the first chunk
@@ -383,6 +431,8 @@ def run_sustained(args) -> dict:
             cache.delta_rotate(-oldest)
             r[1].record(stream)
             newest -= oldest
+        if c + 1 < nch:
+            g = capture_graph(lambda: chunk(np.arange(newest + 1, newest + 1 + N_NEW)), side)
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t0
     clk = clocks.stop()
@@ -613,8 +663,9 @@ def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
 
 def run_bf16_cache(args, dev, K, V, Q, kp, vp, bf16_peak: float) -> dict:
     """The same step (chunk + 60-layer delta rotation) on a bf16 ring: the
-    non-FP8 side of the FP8-versus-bf16 cache comparison.  Same inputs, per-
-    kernel events on the launching stream."""
+    non-FP8 side of the FP8-versus-bf16 cache comparison.  Same inputs; steps
+    timed as CUDA graphs like the FP8 step, per-kernel events from steps
+    launched directly."""
     import numpy as np
     import torch
 
@@ -653,21 +704,20 @@ def run_bf16_cache(args, dev, K, V, Q, kp, vp, bf16_peak: float) -> dict:
 
     for _ in range(args.warmup):
         step()
+    graphed_ms(step, 1, stream)
     torch.cuda.synchronize()
     steps = max(1, args.steps // 2)
+    step_ms = graphed_ms(step, steps, stream) / steps
     rec = {"w": [], "a": [], "r": []}
-    t0, t1 = mk()
-    t0.record(stream)
     for _ in range(steps):
         step(rec)
-    t1.record(stream)
     torch.cuda.synchronize()
     cache.sync()
     cache.close()
     mean_us = lambda evs: statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3  # noqa: E731
     w_us, a_us, r_us = mean_us(rec["w"]), mean_us(rec["a"]), mean_us(rec["r"])
     tflops = ATTN_FLOP / (a_us * 1e-6) / 1e12
-    return {"ms_per_step": round(t0.elapsed_time(t1) / steps, 4), "steps": steps,
+    return {"ms_per_step": round(step_ms, 4), "steps": steps,
             "write_us": round(w_us, 3), "write_gbs": round(BF16_WRITE_BYTES / (w_us * 1e-6) / 1e9, 1),
             "attention_us": round(a_us, 3), "attention_tflops": round(tflops, 1),
             "attention_frac_bf16": round(tflops / bf16_peak, 4),

@@ -32,6 +32,17 @@
  *   - Layouts: K, V and Q are bf16, token-major [n][heads][head_dim] with
  *     head_dim contiguous.  The attention output is fp32 with the same layout.
  *     head_dim is 64 or 128.
+ *   - CUDA graphs: rc_cache_write, rc_attend and rc_cache_delta_rotate only
+ *     launch kernels on `stream` once each has been called directly on the
+ *     device (the first call sets kernel attributes), so a run of them can be
+ *     captured into a graph.  A write to capture must have consecutive
+ *     positions (p0, p0 + 1, ...) or repeat the positions of a recent write:
+ *     any other position vector goes to the device through a pinned buffer
+ *     guarded by an event, which a capture cannot hold.  The host-side
+ *     bookkeeping (slots, write groups, the positions the next attention
+ *     rotates its queries at) is done when a call is captured, and the graph
+ *     keeps that call's arguments: launch each captured graph once, in the
+ *     order of capture, with no direct call on the handle in between.
  */
 #ifndef RC_H
 #define RC_H
