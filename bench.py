@@ -152,24 +152,24 @@ def capture_graph(fn, side):
     return g
 
 
-def graphed_ms(fn, n: int, stream) -> float:
+def graphed_ms(fn, n: int, stream, ahead: bool = False) -> float:
     """Device time of n calls of fn, each captured into its own CUDA graph and
     launched once on `stream`: the host captures call i + 1 while the GPU runs
-    call i, and the first graph is captured before the clock starts.  Events
-    on `stream` bracket the n launches."""
+    call i, and the first graph is captured before the clock starts (ahead:
+    all n are captured first, for calls whose host side is slower than their
+    kernels).  Events on `stream` bracket the n launches."""
     import torch
 
     side = torch.cuda.Stream()
+    todo = [capture_graph(fn, side) for _ in range(n if ahead else 1)]
     done = []
-    g = capture_graph(fn, side)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(n):
+        g = todo[i] if ahead else (todo[0] if i == 0 else capture_graph(fn, side))
         with torch.cuda.stream(stream):
             g.replay()
         done.append(g)
-        if i + 1 < n:
-            g = capture_graph(fn, side)
     t1.record(stream)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1)
@@ -250,7 +250,25 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     cache.sync()
     launches = cache.launch_count - launches0
 
-    # ---- per-kernel times: K more steps launched directly, events around every call
+    # ---- per-kernel times.  Attention and write: the chunk's 240 calls of one
+    # kind captured into a graph and launched back to back, events around the
+    # graphs (an event inside a graph, or around a direct call, widens every
+    # span it brackets); K graphs each, all captured before the clock starts
+    # (the host side of 240 writes takes longer than their kernels).  Also an event pair around every call
+    # in K more steps launched directly (the rotation's time comes from there).
+    def calls(kind):
+        def run():
+            for pas in range(PASSES):
+                for layer in range(L):
+                    if kind == "attend":
+                        cache.attend(layer, Q[pas, layer], out)
+                    else:
+                        cache.write(layer, K[pas, layer], V[pas, layer], chunk_pos)
+        return run
+
+    per_call = 1e3 / (args.steps * CALLS_PER_CHUNK)
+    att_us = graphed_ms(calls("attend"), args.steps, stream, ahead=True) * per_call
+    w_us = graphed_ms(calls("write"), args.steps, stream, ahead=True) * per_call
     nw = args.steps * CALLS_PER_CHUNK
     rec = {"w": [(ev(), ev()) for _ in range(nw)], "a": [(ev(), ev()) for _ in range(nw)],
            "r": [(ev(), ev()) for _ in range(args.steps)], "i": 0, "j": 0}
@@ -294,9 +312,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     hbm = peaks["hbm_gbs"]
     ms_step = elapsed_ms / args.steps
     value = job_throughput(world, args.steps, elapsed_ms)
-    att_us = statistics.mean(a_times)
     achieved_tflops = ATTN_FLOP / (att_us * 1e-6) / 1e12
-    w_us = statistics.mean(w_times)
     r_us = statistics.mean(r_times)
     tr = TRAFFIC["attention"]
     traffic = tr["bytes"] if tr["bytes"] is not None and tr["src_sha256"] == src_sha("rc_attention.cu") else None
@@ -321,7 +337,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "l2": "no flush: 4.3 GB of rings and 6.7 GB of chunk inputs per step exceed the 129 MB L2",
             "parallelism": f"replicas x{world} (one session per GPU)",
             "launch": "each step captured into a CUDA graph (the host captures step k + 1 while the GPU runs "
-                      "step k) and launched once; per-kernel times from as many steps launched directly",
+                      "step k) and launched once",
+            "kernel_times": "attention and write: mean over the chunk's 240 calls of one kind launched back to "
+                            "back in a graph, events around the graph; rotation: events around the call in "
+                            "steps launched directly",
         },
         "ms_per_chunk": round(chunk_ms, 4),
         "roofline": {
@@ -336,13 +355,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "write": {"us": round(w_us, 3), "bytes": WRITE_BYTES,
                       "gbs": round(WRITE_BYTES / (w_us * 1e-6) / 1e9, 1),
                       "frac_hbm": round(WRITE_BYTES / (w_us * 1e-6) / 1e9 / hbm, 4),
-                      "note": "event span includes the per-write host launch gap"},
+                      "us_event_span_direct": round(statistics.mean(w_times), 3)},
             "delta_rotate": {"us": round(r_us, 3), "bytes": ROTATE_BYTES,
                              "gbs": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9, 1),
                              "frac_hbm": round(ROTATE_BYTES / (r_us * 1e-6) / 1e9 / hbm, 4)},
             "attention": {"us": round(att_us, 3), "tflops": round(achieved_tflops, 1),
                           "frac_fp8": round(achieved_tflops / fp8_peak, 4),
-                          "frac_fp8_sustained": round(achieved_tflops / fp8_peak_sustained, 4)},
+                          "frac_fp8_sustained": round(achieved_tflops / fp8_peak_sustained, 4),
+                          "us_event_span_direct": round(statistics.mean(a_times), 3)},
             "readtime_ablation": ab,
             "fused_write": fused,
             "bf16_cache": dict(bf, fp8_ms_per_step=round(ms_step, 4),
