@@ -9,7 +9,9 @@ the 757 queries over all 5,788 slots; then one position reset (delta rotation of
 every stored key in all 60 layers) that moves the window back by one chunk, so
 positions stay in [0, 5788).  That is every step of the path once per step.
 The rings (4.3 GB) and the 240 distinct (K, V, Q) inputs of a chunk (6.7 GB)
-are far larger than L2, so no L2 flush is needed between steps.
+are far larger than L2, so no L2 flush is needed between steps.  Each timed
+step's 481 launches are captured into a CUDA graph (the calls launch kernels
+only) while the GPU runs the previous step, and the graph is launched once.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --sustained 3600    # per-head std U[0.5, 4], restart every 300 chunks: mean / p99 ms per chunk
