@@ -1,7 +1,8 @@
 // rc_rotate.cu -- whole-ring requantisation kernels.
 //
-// K3 rotate_kernel (paperdot abstract: "a delta rotation when positions
-//    reset"): every stored key moves from position p to p + delta in place.
+// K3 rotate_kernel (paperdot abstract: a reset of the positions rotates the
+//    stored keys by the difference): every stored key moves from position p to
+//    p + delta in place.
 //    One cluster of 8 CTAs per (layer, head); each thread owns one 16-byte
 //    chunk (16 codes) of its rows, dequantises and rotates it by delta, and
 //    keeps a running amax per write group that it flushes into a shared-memory

@@ -1,6 +1,6 @@
-// rc_write.cu -- the write path (paperdot abstract: "RoPE and FP8 quantization
-// applied once per write"; cpdf.ai "Como rodar 57B em tempo real com batch
-// size 1": the work moves from read time to write time).
+// rc_write.cu -- the write path (paperdot abstract: keys get RoPE and FP8
+// quantisation a single time, as they are written; cpdf.ai "Como rodar 57B em
+// tempo real com batch size 1": the work moves from read time to write time).
 //
 // K1 rope_table_kernel: cos/sin of p * theta_i for the n positions of a write,
 //    angle formed in fp64 so large positions keep full accuracy.

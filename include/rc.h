@@ -3,10 +3,10 @@
  *
  * The operations come from the pages about "Runway Characters: Serving a 57B
  * Video Diffusion Transformer for Real-Time Conversation" (arXiv 2611.05642):
- *   - paperdot abstract mirror: "a ring cache, RoPE and FP8 quantization
- *     applied once per write, and a delta rotation when positions reset";
- *     each chunk makes 240 attention calls that read a 5,788-slot cache in
- *     which 757 tokens are new.
+ *   - paperdot abstract mirror: the cache is a ring; keys get RoPE and FP8
+ *     quantisation a single time, when written; a reset of the positions
+ *     rotates the stored keys by the difference.  A chunk's 240 attention
+ *     calls each read 5,788 slots, 757 of them new.
  *   - cpdf.ai blog, section "Como rodar 57B em tempo real com batch size 1":
  *     rotary positions and FP8 quantisation move from read time to write
  *     time, and the ring advances the window without copies.
@@ -110,8 +110,8 @@ typedef struct rc_cache rc_cache; /* opaque; owns all of its memory */
 int rc_cache_create(const rc_config *cfg, int device, rc_cache **out);
 
 /*
- * Write n new tokens into ring `layer` (paperdot abstract: "RoPE and FP8
- * quantization applied once per write").  K_bf16 and V_bf16 are device
+ * Write n new tokens into ring `layer` (paperdot abstract: RoPE and FP8
+ * quantisation happen here, a single time per token).  K_bf16 and V_bf16 are device
  * pointers to [n][heads][head_dim] bf16.  positions is a HOST array of n
  * int64 token positions (any sign).  Token t goes to slot
  * floormod(positions[t] - delta_total, slots), replacing what was there.
@@ -128,8 +128,8 @@ int rc_cache_write(rc_cache *h, int layer, const void *K_bf16, const void *V_bf1
                    const int64_t *positions, int n, void *stream);
 
 /*
- * Position reset (paperdot abstract: "a delta rotation when positions
- * reset").  Every occupied slot of every layer moves from position p to
+ * Position reset (paperdot abstract: resetting the positions rotates the
+ * stored keys by the difference).  Every occupied slot of every layer moves from position p to
  * p + delta without moving slots: the stored keys are dequantised, rotated
  * by delta, and each (layer, head, write group) is requantised in place with
  * a fresh scale from its new amax.  Values are untouched.  The layers' last

@@ -13,8 +13,9 @@ and imports nothing from it.
 
 Sources: the pages about "Runway Characters: Serving a 57B Video Diffusion
 Transformer for Real-Time Conversation" (arXiv 2611.05642): the paperdot
-abstract mirror (ring cache, RoPE and FP8 applied once per write, delta
-rotation on position reset, 757 new tokens over 5,788 slots) and the cpdf.ai
+abstract mirror (the cache as a ring; keys quantised to FP8 after RoPE a
+single time, at write; stored keys rotated by the difference when positions reset; 757 new
+tokens among 5,788 slots) and the cpdf.ai
 blog sections "Como rodar 57B em tempo real com batch size 1" (write time
 instead of read time, ring without copies) and "Blackwell, escalabilidade e
 limites do decodificador" (per-head scales).  The readings of what the pages

@@ -9,10 +9,10 @@
  *
  * Sources (web pages about "Runway Characters: Serving a 57B Video Diffusion
  * Transformer for Real-Time Conversation", arXiv 2611.05642):
- *   - paperdot mirror of the arXiv abstract: the cache is a ring, RoPE and
- *     FP8 quantisation are applied once per write, and a delta rotation is
- *     applied when positions reset; 240 attention calls per chunk read a
- *     5,788-slot cache in which 757 tokens are new.
+ *   - paperdot mirror of the arXiv abstract: a ring cache; keys take RoPE
+ *     and FP8 quantisation a single time, when written; resetting the
+ *     positions rotates the stored keys by the difference; each chunk's 240
+ *     attention calls read 5,788 slots, 757 of them new.
  *   - cpdf.ai blog, section "Como rodar 57B em tempo real com batch size 1":
  *     rotary positions and FP8 quantisation are applied when a frame enters
  *     the cache, and the cache is a ring so the window advances without
