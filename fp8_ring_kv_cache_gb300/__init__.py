@@ -21,7 +21,8 @@ Every call is stream-ordered on torch's current stream (or ``stream=``); no
 call after construction allocates device memory.
 """
 from ._binding import (  # noqa: F401
-    EMPTY, RC_ERR_ARG, RC_ERR_CUDA, RC_ERR_OOM, RC_ERR_STATE, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED,
+    EMPTY, RC_BUILD_BOUNDS_CHECK, RC_ERR_ARG, RC_ERR_BOUNDS, RC_ERR_CUDA, RC_ERR_OOM, RC_ERR_STATE, RC_ERR_TIMEOUT,
+    RC_ERR_UNSUPPORTED, rc_build_flags,
     RC_F_BF16_CACHE, RC_F_COPY_WINDOW, RC_F_READTIME_ABLATION, RC_OK, RcError, RingKVCache, declared_symbols, lib, rc_attend, rc_attend_readtime,
     rc_cache_create, rc_cache_delta_rotate, rc_cache_delta_total, rc_cache_destroy, rc_cache_export,
     rc_cache_export_bf16, rc_cache_export_readtime, rc_cache_launch_count, rc_cache_occupancy, rc_cache_set_wait_limit, rc_cache_sync,

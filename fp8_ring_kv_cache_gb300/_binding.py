@@ -2,7 +2,9 @@
 
 Every function here has the name of the C entry point it calls.  Tensors are
 passed as their device addresses; positions are passed as a host int64 array.
-There is no fallback: if librc.so is missing, importing raises.
+There is no fallback: if the library is missing, importing raises.  With
+RC_BOUNDS_CHECK=1 in the environment the bounds-checked build librc_bounds.so
+is loaded instead (same entry points; see rc_build_flags).
 """
 from __future__ import annotations
 
@@ -13,7 +15,7 @@ import re
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "librc.so")
+LIB_PATH = os.path.join(_HERE, "librc_bounds.so" if os.environ.get("RC_BOUNDS_CHECK") == "1" else "librc.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "rc.h")
 
 RC_OK = 0
@@ -23,10 +25,14 @@ RC_ERR_CUDA = -3
 RC_ERR_OOM = -4
 RC_ERR_TIMEOUT = -5
 RC_ERR_UNSUPPORTED = -6
+RC_ERR_BOUNDS = -7
+RC_BUILD_BOUNDS_CHECK = 1
 RC_F_READTIME_ABLATION = 1
 RC_F_COPY_WINDOW = 2
 RC_F_BF16_CACHE = 4
 EMPTY = np.iinfo(np.int64).min
+# bounds-checked build: caches whose index checks or guards failed, found when closed
+BOUNDS_FAILURES: list[str] = []
 
 
 class RcError(RuntimeError):
@@ -63,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "rc_cache_destroy": ([P], None),
         "rc_status_string": ([I], ctypes.c_char_p),
         "rc_cache_sync": ([P], I),
+        "rc_build_flags": ([], ctypes.c_uint),
         "rc_cache_export": ([P, I, P, P, P, P, P, P], I),
         "rc_cache_export_readtime": ([P, P, P, P, P], I),
         "rc_cache_export_bf16": ([P, I, P, P, P, P], I),
@@ -121,6 +128,10 @@ def _dev_ptr(t, dtype, shape, what: str) -> ctypes.c_void_p:
 
 def rc_status_string(status: int) -> str:
     return lib.rc_status_string(int(status)).decode()
+
+
+def rc_build_flags() -> int:
+    return int(lib.rc_build_flags())
 
 
 def rc_cache_create(layers: int, heads: int, head_dim: int, slots: int, max_write: int | None = None,
@@ -261,6 +272,12 @@ class RingKVCache:
 
     def close(self) -> None:
         if getattr(self, "handle", None):
+            if lib.rc_build_flags() & RC_BUILD_BOUNDS_CHECK:
+                # the bounds-checked build: a failed index check or guard that
+                # no sync reported yet is recorded before the handle goes
+                st = lib.rc_cache_sync(self.handle)
+                if st == RC_ERR_BOUNDS:
+                    BOUNDS_FAILURES.append(f"{self.layers}x{self.heads}x{self.head_dim}, {self.slots} slots")
             rc_cache_destroy(self.handle)
             self.handle = None
 

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
     auto stage_ptr = [&](int s) { return smem + Lay::kStage0 + s * Lay::kStageBytes; };
     const uint32_t kv_bytes = Lay::kTile + 1024 + (p.masked ? 512 : 0);
     auto load_tile = [&](int j) {
+        if (!RC_IN_BOUNDS(j >= 0 && j < T, p.status, kSiteAttnTile)) return;
         const int s = j % kStages;
         uint8_t* st = stage_ptr(s);
         uint64_t* full = &bars[B_KV_FULL + s];
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         const int rows_here = min(kRowsPerCta, p.n - row0);
         for (int u = tid; u < rows_here * kUnits; u += kAttnThreads) {
             const int rr = u / kUnits, c = u - rr * kUnits;
+            if (!RC_IN_BOUNDS(rr < kRowsPerCta && row0 + rr < p.n, p.status, kSiteAttnQuery)) continue;
             cp_async16(qstage + rr * (D * 2) + ((c ^ (rr & 7)) << 4),
                        p.q + (static_cast<size_t>(row0 + rr) * p.H + h) * D + c * 8);
         }
@@ -821,7 +823,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
                 for (int i = 0; i < 8; ++i) {
                     const int r = 4 * i + (lane >> 3), q = lane & 7;  // row r of the warp, float4 q
                     const float4 val = *reinterpret_cast<const float4*>(stage + r * 36 + 4 * q);
-                    if (wrow0 + r < p.n)
+                    if (wrow0 + r < p.n && RC_IN_BOUNDS(wrow0 + r >= 0, p.status, kSiteAttnOut))
                         *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(wrow0 + r) * p.H + h) * D + 32 * c +
                                                    4 * q) = val;
                 }
@@ -841,6 +843,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AttnParams p) {
         uint8_t* v16 = smem + Lay::kV16;
         const uint8_t* vhead = p.vt + static_cast<size_t>(h) * T * Lay::kTile;
         auto fetch = [&](int hh, uint4 (&r)[kHalf]) {
+            if (!RC_IN_BOUNDS((hh >> 1) < T, p.status, kSiteAttnVt)) return;
             const uint8_t* src = vhead + static_cast<size_t>(hh >> 1) * Lay::kTile;
 #pragma unroll
             for (int k = 0; k < kHalf; ++k)

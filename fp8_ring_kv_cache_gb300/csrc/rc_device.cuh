@@ -102,6 +102,20 @@ struct AbortState {
 // the teardown drains, which must outlast any MMA or copy still in flight.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Index checks of the bounds-checked build (-DRC_BOUNDS_CHECK): a failed check
+// records kDevBoundsBase + site in the status word (the first failure wins) and
+// the caller skips the access; nothing traps.  In the normal build a check is
+// the constant true and its condition is not evaluated.
+#ifdef RC_BOUNDS_CHECK
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status, int site) {
+    if (!ok && status != nullptr) atomicCAS(status, 0, 200 + site);  // kDevBoundsBase + site
+    return ok;
+}
+#define RC_IN_BOUNDS(cond, status, site) (::rc::bounds_ok((cond), (status), (site)))
+#else
+#define RC_IN_BOUNDS(cond, status, site) true
+#endif
+
 __device__ __forceinline__ void abort_wait(AbortState ab, int where) {
     *ab.flag = 1;
     if (ab.status != nullptr) atomicCAS(ab.status, 0, where);

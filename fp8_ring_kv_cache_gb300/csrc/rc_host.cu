@@ -57,6 +57,7 @@ struct rc_cache {
     float* d_sv = nullptr;
     int32_t* d_grp = nullptr;
     int* d_status = nullptr;
+    std::vector<std::pair<void*, size_t>> guarded;  // bounds-checked build: (guarded base, bytes) of each buffer
     __nv_bfloat16* d_kraw = nullptr;
     __nv_bfloat16* d_vraw = nullptr;
     int64_t* d_slot_pos = nullptr;   // [L][Cpad] each slot's current position (read-time store)
@@ -107,31 +108,33 @@ int64_t floormod(int64_t a, int64_t m) {
     return r < 0 ? r + m : r;
 }
 
+void dfree(rc_cache* h, void* p);
+
 void free_all(rc_cache* h) {
     if (!h) return;
     cudaSetDevice(h->device);
-    cudaFree(h->d_kc);
-    cudaFree(h->d_vt);
-    cudaFree(h->d_sk);
-    cudaFree(h->d_sv);
-    cudaFree(h->d_grp);
-    cudaFree(h->d_status);
-    cudaFree(h->d_kraw);
-    cudaFree(h->d_vraw);
-    cudaFree(h->d_slot_pos);
-    cudaFree(h->d_rt_rope);
-    cudaFree(h->d_rt_kc);
-    cudaFree(h->d_rt_vt);
-    cudaFree(h->d_rt_sk);
-    cudaFree(h->d_rt_sv);
-    cudaFree(h->d2_kc);
-    cudaFree(h->d2_vt);
-    cudaFree(h->d2_sk);
-    cudaFree(h->d2_sv);
-    cudaFree(h->d2_grp);
+    dfree(h, h->d_kc);
+    dfree(h, h->d_vt);
+    dfree(h, h->d_sk);
+    dfree(h, h->d_sv);
+    dfree(h, h->d_grp);
+    dfree(h, h->d_status);
+    dfree(h, h->d_kraw);
+    dfree(h, h->d_vraw);
+    dfree(h, h->d_slot_pos);
+    dfree(h, h->d_rt_rope);
+    dfree(h, h->d_rt_kc);
+    dfree(h, h->d_rt_vt);
+    dfree(h, h->d_rt_sk);
+    dfree(h, h->d_rt_sv);
+    dfree(h, h->d2_kc);
+    dfree(h, h->d2_vt);
+    dfree(h, h->d2_sk);
+    dfree(h, h->d2_sv);
+    dfree(h, h->d2_grp);
     for (auto& e : h->pool) {
-        cudaFree(e.d_table);
-        cudaFree(e.d_pos);
+        dfree(h, e.d_table);
+        dfree(h, e.d_pos);
         if (e.h_pos) cudaFreeHost(e.h_pos);
         if (e.copied) cudaEventDestroy(e.copied);
     }
@@ -259,10 +262,69 @@ int rope_entry(rc_cache* h, const int64_t* p, int n, cudaStream_t s, int* err) {
     return victim;
 }
 
+// Device buffers.  The bounds-checked build puts each between two guard zones
+// of kGuardBytes filled with kGuardByte (the zone keeps the buffer's 256-byte
+// alignment) and records it, so that rc_cache_sync can find writes past either
+// end; the normal build allocates the buffer alone.
+#ifdef RC_BOUNDS_CHECK
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
+#endif
+
 template <typename T>
-int dmalloc(T** p, size_t count) {
+int dmalloc(rc_cache* h, T** p, size_t count) {
     if (count == 0) count = 1;
-    return cudaMalloc(reinterpret_cast<void**>(p), sizeof(T) * count) == cudaSuccess ? RC_OK : RC_ERR_OOM;
+    const size_t bytes = sizeof(T) * count;
+#ifdef RC_BOUNDS_CHECK
+    unsigned char* base = nullptr;
+    if (cudaMalloc(reinterpret_cast<void**>(&base), bytes + 2 * kGuardBytes) != cudaSuccess) return RC_ERR_OOM;
+    if (cudaMemset(base, kGuardByte, kGuardBytes) != cudaSuccess ||
+        cudaMemset(base + kGuardBytes + bytes, kGuardByte, kGuardBytes) != cudaSuccess) {
+        cudaFree(base);
+        return RC_ERR_OOM;
+    }
+    h->guarded.push_back({base, bytes});
+    *p = reinterpret_cast<T*>(base + kGuardBytes);
+    return RC_OK;
+#else
+    (void)h;
+    return cudaMalloc(reinterpret_cast<void**>(p), bytes) == cudaSuccess ? RC_OK : RC_ERR_OOM;
+#endif
+}
+
+// Free a buffer from dmalloc (nullptr is ignored).
+void dfree(rc_cache* h, void* p) {
+    if (p == nullptr) return;
+#ifdef RC_BOUNDS_CHECK
+    unsigned char* base = static_cast<unsigned char*>(p) - kGuardBytes;
+    for (auto& g : h->guarded)
+        if (g.first == base) {
+            g.first = nullptr;
+            cudaFree(base);
+            return;
+        }
+#endif
+    (void)h;
+    cudaFree(p);
+}
+
+// RC_ERR_BOUNDS if a guard zone of any buffer changed (bounds-checked build).
+int check_guards(rc_cache* h) {
+#ifdef RC_BOUNDS_CHECK
+    std::vector<unsigned char> buf(kGuardBytes);
+    for (const auto& g : h->guarded) {
+        if (g.first == nullptr) continue;
+        const unsigned char* base = static_cast<const unsigned char*>(g.first);
+        for (const unsigned char* zone : {base, base + kGuardBytes + g.second}) {
+            if (cudaMemcpy(buf.data(), zone, kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
+            for (unsigned char c : buf)
+                if (c != kGuardByte) return RC_ERR_BOUNDS;
+        }
+    }
+#else
+    (void)h;
+#endif
+    return RC_OK;
 }
 
 int check_sticky() {
@@ -283,6 +345,7 @@ const char* rc_status_string(int status) {
         case RC_ERR_OOM: return "out of device memory";
         case RC_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
         case RC_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case RC_ERR_BOUNDS: return "an index check or a buffer guard failed (bounds-checked build)";
         default: return "unknown status";
     }
 }
@@ -326,7 +389,7 @@ int rc_cache_create(const rc_config* cfg, int device, rc_cache** out) {
     const FaultPlan fault = fault_plan();
     int alloc_no = 0;
     auto injected = [&]() { return fault.alloc_at > 0 && ++alloc_no == fault.alloc_at; };
-    auto dmalloc = [&](auto** p, size_t count) { return injected() ? RC_ERR_OOM : ::dmalloc(p, count); };
+    auto dmalloc = [&](auto** p, size_t count) { return injected() ? RC_ERR_OOM : ::dmalloc(h, p, count); };
     st |= dmalloc(&h->d_kc, rb);
     st |= dmalloc(&h->d_vt, rb);
     st |= dmalloc(&h->d_sk, sc);
@@ -805,9 +868,17 @@ int rc_cache_sync(rc_cache* h) {
     if (cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RC_ERR_CUDA;
     if (st != 0) {
         cudaMemset(h->d_status, 0, sizeof(int));
-        return RC_ERR_TIMEOUT;
+        return (st >= rc::kDevBoundsBase && st < rc::kDevBoundsBase + 100) ? RC_ERR_BOUNDS : RC_ERR_TIMEOUT;
     }
-    return RC_OK;
+    return check_guards(h);
+}
+
+unsigned rc_build_flags(void) {
+#ifdef RC_BOUNDS_CHECK
+    return RC_BUILD_BOUNDS_CHECK;
+#else
+    return 0u;
+#endif
 }
 
 static int export_ring(rc_cache* h, const uint8_t* d_kc, const uint8_t* d_vt, const float* d_sk, const float* d_sv,

@@ -160,6 +160,22 @@ enum DeviceStatus : int {
     kDevTimeoutSoftmax = 103,
     kDevTimeoutConvert = 104,
     kDevTimeoutEpilogue = 105,
+    kDevBoundsBase = 200,  // + the site of a failed index check (bounds-checked build only)
+};
+
+// Sites of the bounds-checked build's index checks (kDevBoundsBase + site).
+enum BoundsSite : int {
+    kSiteWriteStage = 1,   // K2: a token's K, V rows staged from the inputs
+    kSiteWriteRope = 2,    // K2: a token's cos/sin row
+    kSiteWriteSlot = 3,    // K2: a token's slot (codes, scales, group, read-time store)
+    kSiteWriteVStage = 4,  // K2: the shared-memory V staging row
+    kSiteRotCopy = 10,     // K3 staged: the CTA's tiles, scales and groups copied in
+    kSiteRotRow = 11,      // K3: a row's codes, scale or position stored back
+    kSiteRotGroup = 12,    // K3: a write group's amax table entry
+    kSiteAttnTile = 20,    // K4: a K tile with its scales (and groups) copied in
+    kSiteAttnQuery = 21,   // K4: a query row read
+    kSiteAttnVt = 22,      // K4: a Vt tile read by the converter warps
+    kSiteAttnOut = 23,     // K4: an output row stored
 };
 
 }  // namespace rc

@@ -91,7 +91,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
     constexpr int CPR = D / 16;                 // 16-byte chunks per row
     constexpr int RPI = kRotThreads / CPR;      // rows per pass of the CTA
     extern __shared__ __align__(16) uint32_t gmax[];  // [Cpad] group amax (fp32 bits)
-    (void)status;
+    (void)status;  // read by the bounds-checked build's index checks
 
     const int crank = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
     const int tid = threadIdx.x;
@@ -137,6 +137,8 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
         for (int b = 0; b < kBatch; ++b) {
             const int r = rb + b * RPI;
             grow[b] = (r < nrows) ? ggrp[r] : -1;
+            if (grow[b] >= 0 && !RC_IN_BOUNDS(grow[b] < p.Cpad && tile0 + (r >> 7) < p.T, status, kSiteRotGroup))
+                grow[b] = -1;
             if (grow[b] >= 0) raw[b] = *reinterpret_cast<const uint4*>(chunk_addr(r));
         }
 #pragma unroll
@@ -164,14 +166,16 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
     if (crank != 0) {
         for (int r = tid; r < nrows; r += kRotThreads) {
             const int g = ggrp[r];
-            if (g >= 0 && (r == 0 || ggrp[r - 1] != g)) dsmem_max_u32(map_shared(&gmax[g], 0), gmax[g]);
+            if (g >= 0 && RC_IN_BOUNDS(g < p.Cpad, status, kSiteRotGroup) && (r == 0 || ggrp[r - 1] != g))
+                dsmem_max_u32(map_shared(&gmax[g], 0), gmax[g]);
         }
     }
     cluster_sync();
     if (crank != 0) {
         for (int r = tid; r < nrows; r += kRotThreads) {
             const int g = ggrp[r];
-            if (g >= 0 && (r == 0 || ggrp[r - 1] != g)) gmax[g] = dsmem_ld_u32(map_shared(&gmax[g], 0));
+            if (g >= 0 && RC_IN_BOUNDS(g < p.Cpad, status, kSiteRotGroup) && (r == 0 || ggrp[r - 1] != g))
+                gmax[g] = dsmem_ld_u32(map_shared(&gmax[g], 0));
         }
     }
     cluster_sync();  // rank 0's table is not read after this point
@@ -183,6 +187,9 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
         for (int b = 0; b < kBatch; ++b) {
             const int r = rb + b * RPI;
             grow[b] = (r < nrows) ? ggrp[r] : -1;
+            if (grow[b] >= 0 && !RC_IN_BOUNDS(grow[b] < p.Cpad && tile0 + (r >> 7) < p.T && row0 + r < p.Cpad,
+                                              status, kSiteRotRow))
+                grow[b] = -1;
             if (grow[b] >= 0) raw[b] = *reinterpret_cast<const uint4*>(chunk_addr(r));
         }
 #pragma unroll
@@ -273,6 +280,9 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
 
     // the CTA's tiles are contiguous, and so are their scales and groups:
     // three bulk copies on one barrier
+    const bool copy_ok = RC_IN_BOUNDS(
+        ntiles <= Lay::kMaxTiles && tile0 + ntiles <= p.T && row0 + ntiles * kTileSlots <= p.Cpad, status,
+        kSiteRotCopy);
     if (tid == 0) {
         misc[0] = 0u;
         mbar_init(&bars[0], 1);
@@ -288,7 +298,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
             const uint64_t t0 = global_timer_ns();
             while (global_timer_ns() - t0 < hold) __nanosleep(256);
         }
-        if (ntiles > 0) {
+        if (ntiles > 0 && copy_ok) {
             mbar_arrive_expect_tx(&bars[0], ntiles * (Lay::kTile + 2 * kTileSlots * 4));
             bulk_g2s(codes, gkc, ntiles * Lay::kTile, &bars[0]);
             bulk_g2s(ssk, gsk, ntiles * kTileSlots * 4, &bars[0]);
@@ -344,7 +354,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
     auto flush = [&]() {
         if (gcur >= 0) dsmem_max_u32(map_shared(&tab[gcur >> 3], gcur & 7), __float_as_uint(acc * scur));
     };
-    if (ntiles > 0) ok = mbar_wait(&bars[0], 0, ab, kDevTimeoutLoader);
+    if (ntiles > 0) ok = copy_ok && mbar_wait(&bars[0], 0, ab, kDevTimeoutLoader);
     for (int i = 0; i < ntiles && ok; ++i) {
 #pragma unroll 1
         for (int rb = i * kTileSlots; rb < (i + 1) * kTileSlots; rb += RPP) {
@@ -352,6 +362,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
             const int g0 = (r < nrows) ? sgrp[r] : -1;
             const int g1 = (r + 1 < nrows) ? sgrp[r + 1] : -1;
             if (g0 < 0 && g1 < 0) continue;
+            if (!RC_IN_BOUNDS(g0 < p.Cpad && g1 < p.Cpad, status, kSiteRotGroup)) continue;
             float2 X[8], Y[8];
             rotate_rows(r, X, Y);
             float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
@@ -387,6 +398,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
         for (int r = tid; r < nrows; r += kRotThreads) {
             const int g = sgrp[r];
             if (g < 0) continue;
+            if (!RC_IN_BOUNDS(g < p.Cpad && row0 + r < p.Cpad, status, kSiteRotRow)) continue;
             const float amax = __uint_as_float(dsmem_ld_u32(map_shared(&tab[g >> 3], g & 7)));
             const float snew = (amax > 0.f) ? __fdiv_rn(amax, 448.f) : 1.f;
             gsk[r] = snew;
@@ -421,6 +433,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
             }
             uint32_t o0, o1;
             chunk_off(r, o0, o1);
+            if (!RC_IN_BOUNDS(tile0 + ((r + 1) >> 7) < p.T, status, kSiteRotRow)) continue;
             if (g0 >= 0) *reinterpret_cast<uint4*>(gkc + o0) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
             if (g1 >= 0) *reinterpret_cast<uint4*>(gkc + o1) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
@@ -431,7 +444,7 @@ __global__ void __cluster_dims__(kRotCluster, 1, 1) __launch_bounds__(kRotThread
         for (int r = tid; r < nrows; r += kRotThreads)
             if (sgrp[r] >= 0) spos[r] += p.delta;
     }
-    if (!ok && tid == 0 && ntiles > 0) {
+    if (!ok && copy_ok && tid == 0 && ntiles > 0) {
         // leave no copy in flight into this CTA's shared memory (bounded)
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(&bars[0], 0) && global_timer_ns() - t0 < 100000000ull) {

@@ -110,7 +110,8 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
             const int which = r / kUnits, cc = r - which * kUnits;
             const __nv_bfloat16* src = (which ? p.V : p.K) + (static_cast<size_t>(tb + tl) * p.H + h) * D + cc * 8;
             __nv_bfloat16* dst = (which ? vbuf : kbuf) + tl * D + cc * 8;
-            cp_async16(dst, src);
+            if (RC_IN_BOUNDS(tb + tl >= 0 && tb + tl < p.n && tl < kWriteTB, p.status, kSiteWriteStage))
+                cp_async16(dst, src);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -123,8 +124,9 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
     auto fetch_rope = [&](int tb, int cnt, float4 (&cs)[kSteps][4]) {
 #pragma unroll
         for (int st = 0; st < kSteps; ++st) {
-            const float4* rr =
-                reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(tb + min(tok(st), cnt - 1)) * HALF);
+            const int t = tb + min(tok(st), cnt - 1);
+            const float4* rr = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(t) * HALF);
+            if (!RC_IN_BOUNDS(t >= 0 && t < p.n, p.status, kSiteWriteRope)) rr = reinterpret_cast<const float4*>(p.rope);
             cs[st][0] = __ldg(rr + 2 * c);
             cs[st][1] = __ldg(rr + 2 * c + 1);
             cs[st][2] = __ldg(rr + D / 8 + 2 * c);
@@ -177,6 +179,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
             if (p.kraw != nullptr && tok(st) < cnt) {
                 // read-time ablation store: the unrotated bf16 row and the slot's position
                 const int slot = slot_of(tb + tl);
+                if (!RC_IN_BOUNDS(slot >= 0 && slot < p.C, p.status, kSiteWriteSlot)) continue;
                 uint8_t* kd = reinterpret_cast<uint8_t*>(p.kraw + (static_cast<size_t>(h) * p.Cpad + slot) * D);
                 uint8_t* vd = reinterpret_cast<uint8_t*>(p.vraw + (static_cast<size_t>(h) * p.Cpad + slot) * D);
                 const uint8_t* kr = reinterpret_cast<const uint8_t*>(kbuf + tl * D);
@@ -246,6 +249,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
             float k[16], v[16];
             row(tl, cs[st], k, v);
             const int slot = slot_of(tb + tl);
+            const bool in_range = RC_IN_BOUNDS(slot >= 0 && slot < p.C && tw < kWriteTB, p.status, kSiteWriteSlot);
             uint32_t kq[8], vq[8];  // codes of pairs i (16 bits each)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -254,7 +258,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
                 kq[i] = e4m3x2(a.x, a.y);
                 vq[i] = e4m3x2(bq.x, bq.y);
             }
-            if (live) {
+            if (live && in_range) {
                 uint8_t* ktile = p.kc + static_cast<size_t>(h * p.T + (slot >> 7)) * (kTileSlots * D);
                 *reinterpret_cast<uint2*>(ktile + ktile_off(slot & 127, 8 * c, D)) =
                     make_uint2(kq[0] | (kq[1] << 16), kq[2] | (kq[3] << 16));
@@ -279,6 +283,7 @@ __global__ void __cluster_dims__(kWriteCluster, 1, 1) __launch_bounds__(kWriteTh
         uint8_t* vhead = p.vt + static_cast<size_t>(h) * p.T * (D * kTileSlots);
         for (int tl = lane; tl < cnt; tl += 32) {
             const int slot = sslot[tl];
+            if (!RC_IN_BOUNDS(slot >= 0 && slot < p.C, p.status, kSiteWriteVStage)) continue;
             // Vt byte of (d, slot): tile base + d * 128 + ((chunk ^ (d & 7)) << 4) + (slot & 15)
             uint8_t* base = vhead + static_cast<size_t>(slot >> 7) * (D * kTileSlots) + (slot & 15);
             const int chunk = (slot >> 4) & 7;

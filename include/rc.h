@@ -67,6 +67,10 @@ extern "C" {
                                    its output is not valid */
 #define RC_ERR_UNSUPPORTED (-6) /* shape not supported (head_dim other than 64 or 128,
                                    or a device that is not sm_103) */
+#define RC_ERR_BOUNDS (-7)      /* bounds-checked build only (rc_build_flags): a kernel's
+                                   index check failed and the access was skipped, or a
+                                   buffer's guard bytes were overwritten; results are
+                                   not valid */
 
 /* ---- configuration ------------------------------------------------------ */
 /* Keep the unrotated bf16 K, V of every slot as well, so that rc_attend_readtime
@@ -195,8 +199,21 @@ const char *rc_status_string(int status);
 
 /* ---- inspection and test support -------------------------------------- */
 
-/* Synchronise the handle's last stream and report any kernel error or timeout. */
+/* Synchronise the handle's last stream and report any kernel error or timeout
+   (RC_ERR_TIMEOUT), and in the bounds-checked build a failed index check or
+   overwritten guard bytes (RC_ERR_BOUNDS).  The device status word is cleared. */
 int rc_cache_sync(rc_cache *h);
+
+/* How this library was built: RC_BUILD_BOUNDS_CHECK is set in the bounds-
+   checked build (librc_bounds.so, compiled with -DRC_BOUNDS_CHECK).  There,
+   the write, rotation and attention kernels test the index of each global
+   access they make against the buffer it addresses before making it (a
+   failure skips the access and records the site; nothing traps), and every
+   device buffer of a handle sits between two 256-byte guard zones filled with
+   0xA5 that rc_cache_sync checks.  The normal build has neither and returns 0.
+   Needs no device. */
+#define RC_BUILD_BOUNDS_CHECK 1u
+unsigned rc_build_flags(void);
 
 /*
  * Failure-path support.  Every wait inside the attention kernel is bounded:

@@ -32,9 +32,27 @@ def test_header_declarations_are_the_abi(rc):
     assert set(rc.declared_symbols()) <= exported
 
 
+def test_bounds_checked_build_has_the_same_abi(rc):
+    # librc_bounds.so (-DRC_BOUNDS_CHECK) exports every declared entry point
+    # and says so through rc_build_flags; librc.so reports no checks
+    import os
+    import subprocess
+    here = os.path.dirname(rc._binding.__file__)
+    flags = {}
+    for name in ("librc.so", "librc_bounds.so"):
+        path = os.path.join(here, name)
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+        exported = set(re.findall(r"\bT (rc_\w+)$", out, flags=re.M))
+        assert set(rc.declared_symbols()) <= exported, name
+        lib = ctypes.CDLL(path)
+        lib.rc_build_flags.restype = ctypes.c_uint
+        flags[name] = lib.rc_build_flags()
+    assert flags == {"librc.so": 0, "librc_bounds.so": rc.RC_BUILD_BOUNDS_CHECK}
+
+
 def test_status_strings(rc):
     for st in (rc.RC_OK, rc.RC_ERR_ARG, rc.RC_ERR_STATE, rc.RC_ERR_CUDA, rc.RC_ERR_OOM, rc.RC_ERR_TIMEOUT,
-               rc.RC_ERR_UNSUPPORTED):
+               rc.RC_ERR_UNSUPPORTED, rc.RC_ERR_BOUNDS):
         s = rc.rc_status_string(st)
         assert s and s != "unknown status"
     assert rc.rc_status_string(12345) == "unknown status"
