@@ -5,7 +5,7 @@ compiled with -DRC_BOUNDS_CHECK) stands in for it.  There the write, rotation
 and attention kernels test the index of each checked global access against
 its buffer before making it (a failed check skips the access and records the
 site in the status word; nothing traps), and every device buffer sits between
-two guard zones that rc_cache_sync checks.  The parity suites run in a child
+two guard zones that rc_cache_sync checks.  The GPU suites run in a child
 process with RC_BOUNDS_CHECK=1, so they load that build: a failed check fails
 the test whose sync reports it, and tests/conftest.py fails any test that left
 a cache with an unreported failure when it was closed.  Their shapes include
@@ -43,7 +43,10 @@ def test_child_loads_the_bounds_checked_build(built):
     assert r.returncode == 0, r.stdout + r.stderr
 
 
-@pytest.mark.parametrize("suite", ["tests/test_gpu_parity.py", "tests/test_gpu_graph.py"])
+# the 16-bit and fused-write kernels have no index checks; their suites still
+# run here for the guard zones, which catch a write past either end of any buffer
+@pytest.mark.parametrize("suite", ["tests/test_gpu_parity.py", "tests/test_gpu_graph.py", "tests/test_gpu_bf16.py",
+                                   "tests/test_gpu_fused.py"])
 def test_parity_suite_on_bounds_checked_build(built, suite):
     r = run_child(["-m", "pytest", suite, "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider"], 1500)
     tail = (r.stdout[-4000:] + r.stderr[-2000:])
