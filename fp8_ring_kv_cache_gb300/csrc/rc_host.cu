@@ -16,6 +16,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "rc.h"
 #include "rc_internal.h"
 #include "rc_layout.h"
@@ -173,6 +175,16 @@ void refresh_uniform(rc_cache* h, int layer) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A named NVTX range around each entry point that enqueues work, so that a
+// timeline tool (Nsight Systems, or ncu --nvtx --nvtx-include) shows which
+// call launched which kernels; with no tool attached the calls do nothing.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Host-side fault injection for the failure-path tests, read from the
 // environment at each use: RC_FAULT_INJECT=alloc:K makes the K-th allocation
@@ -588,6 +600,7 @@ static int write_common(rc_cache* h, int layer, const int64_t* positions, int n,
 
 int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf16, const int64_t* positions, int n,
                    void* stream) {
+    const NvtxRange range("rc_cache_write");
     if (!h || !K_bf16 || !V_bf16 || !positions) return RC_ERR_ARG;
     if (!aligned16(K_bf16) || !aligned16(V_bf16)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write) return RC_ERR_ARG;
@@ -603,6 +616,7 @@ int rc_cache_write(rc_cache* h, int layer, const void* K_bf16, const void* V_bf1
 int rc_cache_write_fused(rc_cache* h, int layer, const uint8_t* X, float x_scale, const uint8_t* Wk, float wk_scale,
                          const uint8_t* Wv, float wv_scale, int hidden, const int64_t* positions, int n,
                          void* stream) {
+    const NvtxRange range("rc_cache_write_fused");
     if (!h || !X || !Wk || !Wv || !positions) return RC_ERR_ARG;
     if (!aligned16(X) || !aligned16(Wk) || !aligned16(Wv)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1 || n > h->max_write || n > kFusedMaxTokens) return RC_ERR_ARG;
@@ -623,6 +637,7 @@ int rc_cache_write_fused(rc_cache* h, int layer, const uint8_t* X, float x_scale
 }
 
 int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
+    const NvtxRange range("rc_cache_delta_rotate");
     if (!h) return RC_ERR_ARG;
     if (delta == 0) return RC_OK;
     if (launch_fault()) return RC_ERR_CUDA;
@@ -660,6 +675,7 @@ int rc_cache_delta_rotate(rc_cache* h, int64_t delta, void* stream) {
 }
 
 int rc_cache_window_shift(rc_cache* h, int64_t k, void* stream) {
+    const NvtxRange range("rc_cache_window_shift");
     if (!h || k < 0) return RC_ERR_ARG;
     if (!h->copy_window) return RC_ERR_STATE;
     const int kk = static_cast<int>(k % h->C);
@@ -754,6 +770,7 @@ static int attend_bf16(rc_cache* h, int layer, const void* Q_bf16, float* out, i
 
 static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out, int n, void* stream,
                          bool readtime) {
+    const NvtxRange range(readtime ? "rc_attend_readtime" : "rc_attend");
     if (!h || !Q_bf16 || !out) return RC_ERR_ARG;
     if (!aligned16(Q_bf16) || !aligned16(out)) return RC_ERR_ARG;
     if (layer < 0 || layer >= h->L || n < 1) return RC_ERR_ARG;
