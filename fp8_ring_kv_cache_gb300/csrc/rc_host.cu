@@ -821,6 +821,7 @@ static int attend_common(rc_cache* h, int layer, const void* Q_bf16, float* out,
         rp.C = h->C;
         rp.T = h->T;
         rp.Cpad = h->Cpad;
+        rp.status = h->d_status;
         if (launch_readtime(rp, h->D, s) != cudaSuccess) return RC_ERR_CUDA;
         h->launches += 1;
         ap.kc = h->d_rt_kc;

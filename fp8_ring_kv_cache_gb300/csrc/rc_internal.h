@@ -94,6 +94,7 @@ struct ReadtimeParams {
     float* sk;                  // [H][Cpad]
     float* sv;
     int H, C, T, Cpad;
+    int* status;                // device status word (index checks of the bounds-checked build)
 };
 
 // K4: FP8 attention over one layer's ring (the queries are rotated, scaled
@@ -176,6 +177,8 @@ enum BoundsSite : int {
     kSiteAttnQuery = 21,   // K4: a query row read
     kSiteAttnVt = 22,      // K4: a Vt tile read by the converter warps
     kSiteAttnOut = 23,     // K4: an output row stored
+    kSiteRtRow = 30,       // K5: a slot's unrotated K, V row and its cos/sin read
+    kSiteRtTile = 31,      // K5: a tile's codes and a slot's scales stored
 };
 
 }  // namespace rc

@@ -571,6 +571,7 @@ __global__ void __cluster_dims__(kRtCluster, 1, 1) __launch_bounds__(kRtThreads,
     // ---- phase 1
     float ak = 0.f, av = 0.f;
     for (int r = warp; r < nrows; r += kRtWarps) {
+        if (!RC_IN_BOUNDS(row0 + r < p.Cpad, p.status, kSiteRtRow)) continue;
         if (p.grp[row0 + r] < 0) continue;
         float k[EPL], v[EPL];
         rt_load_row<D>(p, h, row0 + r, dim0, k, v);
@@ -608,6 +609,7 @@ __global__ void __cluster_dims__(kRtCluster, 1, 1) __launch_bounds__(kRtThreads,
         uint8_t* vtile = p.vt + (static_cast<size_t>(h) * p.T + tile) * (kTileSlots * D);
         for (int rr = warp; rr < kTileSlots; rr += kRtWarps) {
             const int slot = tile * kTileSlots + rr;
+            if (!RC_IN_BOUNDS(tile < p.T && slot < p.Cpad, p.status, kSiteRtTile)) continue;
             const bool occ = (slot < p.C) && (p.grp[slot] >= 0);
             uint32_t kcode = 0, vcode = 0;
             if (occ) {

@@ -206,7 +206,7 @@ int rc_cache_sync(rc_cache *h);
 
 /* How this library was built: RC_BUILD_BOUNDS_CHECK is set in the bounds-
    checked build (librc_bounds.so, compiled with -DRC_BOUNDS_CHECK).  There,
-   the write, rotation and attention kernels test the index of each global
+   the write, rotation, read-time and attention kernels test the index of each global
    access they make against the buffer it addresses before making it (a
    failure skips the access and records the site; nothing traps), and every
    device buffer of a handle sits between two 256-byte guard zones filled with

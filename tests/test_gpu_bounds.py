@@ -1,7 +1,7 @@
 """The GPU parity tests again, on the bounds-checked build.
 
 compute-sanitizer is closed on this machine; librc_bounds.so (the same sources
-compiled with -DRC_BOUNDS_CHECK) stands in for it.  There the write, rotation
+compiled with -DRC_BOUNDS_CHECK) stands in for it.  There the write, rotation, read-time
 and attention kernels test the index of each checked global access against
 its buffer before making it (a failed check skips the access and records the
 site in the status word; nothing traps), and every device buffer sits between
