@@ -7,12 +7,15 @@ which can synchronise the device.  rc_ring_write_noalloc writes into a ring the
 caller owns and keeps its only scratch (the RoPE table) in a static device
 array.  Here the test itself allocates that caller-owned ring with torch, makes
 two writes in a row with both entry points on the same inputs, and compares
-codes, scales and groups with the tolerances of the other parity tests.
+codes, scales and groups with the tolerances of the other parity tests --
+against rc_cache_write and, for the consecutive-position writes, against the
+oracle's write as well.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth_inputs as si
 from parity_util import check_codes, check_scales
 
@@ -61,7 +64,9 @@ def test_noalloc_write_matches_cache_write(D):
     from fp8_ring_kv_cache_gb300._binding import rc_ring_write_noalloc
 
     H, C = 8, 1000
+    oracle.build()
     cache = rc.RingKVCache(1, H, D, C)
+    ora = oracle.OracleCache(1, H, D, C)
     ring = _new_ring(H, D, C)
     writes = [(0, 600, 0.5), (600, 500, 3.0)]   # the second write wraps onto slots 0..99
     inputs = []
@@ -72,6 +77,7 @@ def test_noalloc_write_matches_cache_write(D):
     torch.cuda.synchronize()
     for i, (k, v, pos) in enumerate(inputs):
         cache.write(0, k, v, pos)
+        ora.write(0, k.cpu(), v.cpu(), pos)
         free_before = torch.cuda.mem_get_info()[0]
         rc_ring_write_noalloc(ring, k, v, pos, delta_total=0, group=i)
         torch.cuda.synchronize()
@@ -88,6 +94,13 @@ def test_noalloc_write_matches_cache_write(D):
         # the slots of write j carry group j; untouched slots stay empty
         assert np.array_equal(got["group"][occ], want["gid"][occ].astype(np.int32))
         assert (got["group"][~occ] == -1).all()
+        # and the oracle's write of the same tokens
+        ref = ora.export(0)
+        assert np.array_equal(ref["pos"] != oracle.EMPTY, occ)
+        check_codes(got["kcodes"][:, occ], ref["kcodes"][:, occ], f"write {i} K codes vs oracle")
+        check_codes(got["vcodes"][:, occ], ref["vcodes"][:, occ], f"write {i} V codes vs oracle")
+        check_scales(got["kscale"][:, occ], ref["kscale"][:, occ], f"write {i} K scales vs oracle")
+        check_scales(got["vscale"][:, occ], ref["vscale"][:, occ], f"write {i} V scales vs oracle")
     cache.close()
 
 
