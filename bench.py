@@ -289,7 +289,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     del cache
 
     # ---- read-time ablation: same chunk, whole-cache RoPE + quantisation per call
-    ab = run_ablation(args, dev, K, V, Q, mult, seed, kp, vp)
+    ab = run_ablation(args, dev, K, V, Q, kp, vp)
 
     # ---- the same step on a bf16 ring (the FP8-versus-bf16 cache comparison)
     peaks, peak_src = load_peaks()
@@ -299,7 +299,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     fused = run_fused(args, dev, 2.0 * peaks["bf16_tflops"])
 
     # ---- end to end through the C ABI with host buffers
-    e2e = run_e2e(args, dev, K, V, Q, mult, kp, vp)
+    e2e = run_e2e(args, dev, K, V, Q, kp, vp)
 
     # ---- max over ranks
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["elapsed_ms"]], dev, world)
@@ -640,7 +640,7 @@ def run_copy_window(args) -> dict:
     }
 
 
-def run_ablation(args, dev, K, V, Q, mult, seed, kp, vp) -> dict:
+def run_ablation(args, dev, K, V, Q, kp, vp) -> dict:
     import numpy as np
     import torch
 
@@ -811,7 +811,7 @@ def run_fused(args, dev, fp8_peak: float) -> dict:
     return res
 
 
-def run_e2e(args, dev, K, V, Q, mult, kp, vp) -> dict:
+def run_e2e(args, dev, K, V, Q, kp, vp) -> dict:
     """The same step as the device-timed one (a 240-call chunk, then the
     60-layer delta rotation that restarts the window) through the public API
     with pinned host inputs: every call copies its K, V, Q host->device and its

@@ -12,12 +12,6 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
 
 
-def pytest_collection_modifyitems(config, items):
-    # GPU tests cannot run without a device; fail loudly instead of skipping
-    # when the marker is selected explicitly and no GPU exists.
-    pass
-
-
 @pytest.fixture(scope="session")
 def oracle_mod():
     import oracle
